@@ -1,0 +1,489 @@
+"""Benchmark of the spatial-transformer sampling path on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--dtype DT] [--no-extra]
+
+A step is one pass of the hot path over one batch: by default the fused
+AffineGrid+GridSample 2-D workload "stn2d" -- theta (64,2,3) = identity +
+N(0,0.1), X (64,32,128,128) ~ N(0,1) fp32, output 128x128, linear, border,
+align_corners=1 -- one gs_affine_sample call.  Inputs are seeded synthetic
+data resident in HBM before the timed region; L2 is flushed (a 512 MiB write)
+before every timed step, outside the step's CUDA-event interval.  Time is
+taken with CUDA events on the stream the kernel runs on; the timed region is
+bracketed by barrier + synchronize, and the max over ranks is reported.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the images are independent; there is no exchange step) and `value` is the
+whole job's output elements per second.
+
+--impl reference times the CPU oracle (plain C, fp64, OpenMP over output
+elements) on a bounded sample of the same workload and prints the same JSON
+line with "impl": "reference".
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from spatial_transformer_sampling_gb300 import workloads as wl  # noqa: E402
+
+DT_SHORT = {"float32": "f32", "float16": "f16", "bfloat16": "bf16"}
+DT_BYTES = {"float32": 4, "float16": 2, "bfloat16": 2}
+METRIC = "GridSample output elems/s (achieved HBM GB/s in roofline)"
+UNIT = "elems/s"
+
+
+# ------------------------------------------------------------------ helpers
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="stn2d")
+    p.add_argument("--dtype", default="float32")
+    p.add_argument("--mode", default=None, help="override the workload's mode")
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    p.add_argument("--extra-steps", type=int, default=100)
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_source_sha():
+    """Hash of the CUDA sources: ncu traffic figures are valid only for this exact code."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "spatial_transformer_sampling_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_tag, workload, dtype):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(item.split("=", 1) for item in line.split())
+        if (kv.get("kernel") == kernel_tag and kv.get("workload") == workload
+                and kv.get("dtype") == dtype and kv.get("src_sha") == sha):
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples for one GPU, with timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(inside) < 2:   # a short region: keep the samples around it
+            inside = [p for t, p in self.samples if t0 - 1.0 <= t <= t1 + 1.0]
+            window = "timed region +- 1 s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][1]), "reasons": reasons, "samples": len(inside),
+                "window": window}
+
+
+# --------------------------------------------------------------- workloads
+
+class Case:
+    """One workload on one device: inputs in HBM, a launch closure, byte/flop counts."""
+
+    def __init__(self, name, dtype, device, mode=None, seed_offset=0):
+        import torch
+        self.w = wl.WORKLOADS[name]
+        self.name, self.dtype, self.device = name, dtype, device
+        self.mode = mode or self.w.mode
+        w = self.w
+        eb = DT_BYTES[dtype]
+        seed = w.seed + seed_offset
+        import spatial_transformer_sampling_gb300 as gs
+        self.gs = gs
+        if w.kind == "affine_sample":
+            inp = wl.make_affine_sample_inputs(w, seed=seed)
+            self.host = {"theta": wl.as_dtype(inp["theta"], dtype), "X": wl.as_dtype(inp["X"], dtype)}
+            self.size = [int(s) for s in inp["size"]]
+            self.outputs = int(np.prod(self.size))
+            self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},affine>"
+        elif w.kind == "grid_sample":
+            inp = wl.make_grid_sample_inputs(w, seed=seed)
+            self.host = {"X": wl.as_dtype(inp["X"], dtype), "grid": wl.as_dtype(inp["grid"], dtype)}
+            self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
+            self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},grid>"
+        else:
+            inp = wl.make_deform_inputs(w, seed=seed)
+            self.host = {k: wl.as_dtype(v, dtype) for k, v in inp.items()}
+            N, C, H, W_ = w.x_shape
+            oH = (H + w.pads[0] + w.pads[2] - (w.kernel[0] - 1) - 1) // w.strides[0] + 1
+            oW = (W_ + w.pads[1] + w.pads[3] - (w.kernel[1] - 1) - 1) // w.strides[1] + 1
+            self.outputs = N * w.oc * oH * oW
+            self.flops = 2.0 * N * oH * oW * w.oc * (C // w.group) * w.kernel[0] * w.kernel[1]
+            self.kernel_tag = f"deform<{DT_SHORT[dtype]}>"
+        self.dev = {k: v.to(device) for k, v in self.host.items()}
+        self.out = torch.empty(self._out_shape(), dtype=self.dev["X"].dtype, device=device)
+        # algorithmic bytes: every input read once, the output written once
+        self.bytes = sum(t.numel() for t in self.host.values()) * eb + self.outputs * eb
+
+    def _out_shape(self):
+        w = self.w
+        if w.kind == "affine_sample":
+            return self.size
+        if w.kind == "grid_sample":
+            return list(w.x_shape[:2]) + list(w.out_spatial)
+        N, C, H, W_ = w.x_shape
+        return [N, w.oc, H, W_]
+
+    def run(self, dev=None, out=None):
+        d = dev or self.dev
+        out = self.out if out is None else out
+        w = self.w
+        if w.kind == "affine_sample":
+            return self.gs.gs_affine_sample(d["theta"], self.size, d["X"], self.mode,
+                                            w.padding_mode, w.align_corners, w.cubic_coeff_a,
+                                            out=out)
+        if w.kind == "grid_sample":
+            return self.gs.gs_grid_sample(d["X"], d["grid"], self.mode, w.padding_mode,
+                                          w.align_corners, w.cubic_coeff_a, out=out)
+        return self.gs.gs_deform_conv(d["X"], d["W"], d["offset"], d["B"], d["mask"],
+                                      kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
+                                      dilations=w.dilations, group=w.group,
+                                      offset_group=w.offset_group, out=out)
+
+
+def time_steps(case, steps, warmup, flush, barrier=None):
+    """Per-step CUDA-event durations (ms) of the hot path, L2 flushed before each step."""
+    import torch
+    stream = torch.cuda.current_stream(case.device)
+    for _ in range(warmup):
+        flush.zero_()
+        case.run()
+    torch.cuda.synchronize(case.device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize(case.device)
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        case.run()
+        ends[i].record(stream)
+    torch.cuda.synchronize(case.device)
+    if barrier:
+        barrier()
+    t1 = time.time()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1
+
+
+def time_e2e(case, steps, warmup):
+    """Host buffers in, host buffer out: pinned H2D copies, the call, D2H of Y, per step."""
+    import torch
+    stream = torch.cuda.current_stream(case.device)
+    pinned = {k: v.pin_memory() for k, v in case.host.items()}
+    out_host = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    d = {k: torch.empty_like(v, device=case.device) for k, v in case.host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k in d:
+            d[k].copy_(pinned[k], non_blocking=True)
+        case.run(dev=d)
+        out_host.copy_(case.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(case.device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    e.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+def roofline_for(case, ms, pk):
+    if case.w.kind == "deform_conv" and case.dtype != "float32":
+        achieved = case.flops / (ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(case.kernel_tag, case.name, case.dtype),
+                "peak_source": pk["source"]}
+    achieved = case.bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4),
+            "traffic": recorded_traffic(case.kernel_tag, case.name, case.dtype),
+            "algorithmic_bytes": case.bytes, "peak_source": pk["source"]}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(case, budget_s=12.0):
+    """Time the oracle on a bounded slice of the workload: whole images, grown until ~budget_s."""
+    import oracle
+    w = case.w
+    threads = oracle.max_threads()
+    oracle.set_num_threads(threads)
+    h = {k: wl.widened(v) for k, v in case.host.items()}
+    total_t, total_out, images = 0.0, 0, 0
+    n_img = 1
+    while total_t < budget_s and images < w.x_shape[0]:
+        n = min(n_img, w.x_shape[0] - images)
+        sl = slice(images, images + n)
+        t = time.perf_counter()
+        if w.kind == "affine_sample":
+            size = [n] + case.size[1:]
+            Y = oracle.affine_sample(h["theta"][sl], size, h["X"][sl], case.mode, w.padding_mode,
+                                     w.align_corners, w.cubic_coeff_a)
+        elif w.kind == "grid_sample":
+            Y = oracle.grid_sample(h["X"][sl], h["grid"][sl], case.mode, w.padding_mode,
+                                   w.align_corners, w.cubic_coeff_a)
+        else:
+            Y = oracle.deform_conv(h["X"][sl], h["W"], h["offset"][sl], h["B"], h["mask"][sl],
+                                   kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
+                                   dilations=w.dilations, group=w.group,
+                                   offset_group=w.offset_group)
+        total_t += time.perf_counter() - t
+        total_out += Y.size
+        images += n
+        n_img *= 2
+    return {"value": total_out / total_t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {images} of {w.x_shape[0]} images of {case.name} "
+                      f"({total_out} outputs, {total_t:.1f} s, fp64 C, OpenMP {threads} threads)"}
+
+
+# ------------------------------------------------------------------- main
+
+def workload_desc(case):
+    w = case.w
+    if w.kind == "affine_sample":
+        return (f"{case.name}: fused AffineGrid+GridSample {w.r}-D, theta ({w.x_shape[0]},{w.r},"
+                f"{w.r + 1}) = identity + N(0,{w.theta_noise}), X {tuple(w.x_shape)} ~ N(0,1) "
+                f"{case.dtype}, out {tuple(w.out_spatial)}, {case.mode}, {w.padding_mode}, "
+                f"align_corners={w.align_corners}")
+    if w.kind == "grid_sample":
+        return (f"{case.name}: GridSample {w.r}-D, X {tuple(w.x_shape)} {w.x_dist}, grid "
+                f"({w.x_shape[0]},{','.join(map(str, w.out_spatial))},{w.r}) {w.grid_dist}, "
+                f"{case.dtype}, {case.mode}, {w.padding_mode}, align_corners={w.align_corners}")
+    return (f"{case.name}: DeformConv 2-D, X {tuple(w.x_shape)}, W ({w.oc},{w.x_shape[1]},3,3), "
+            f"pads 1, stride 1, offset/mask from N(0,1), {case.dtype}")
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    __graft_entry__.build()
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    barrier = None
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+        barrier = dist.barrier
+    pk = peaks()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    case = Case(args.workload, args.dtype, device, args.mode, seed_offset=rank)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        time.sleep(0.6)   # let nvidia-smi start reporting before the timed region
+    per_step, t0, t1 = time_steps(case, args.steps, args.warmup, flush, barrier)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+    ms = sum(per_step) / len(per_step)
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = case.outputs * world / (ms_max * 1e-3)
+
+    e2e_ms, h2d, d2h = time_e2e(case, max(5, min(50, args.steps // 10)), 3)
+    e2e_value = case.outputs * world / (e2e_ms * 1e-3)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = case.outputs * world / (float(t.item()) * 1e-3)
+
+    extra = []
+    if rank == 0 and not args.no_extra:
+        for name, dt, mode in (("stn2d", "bfloat16", None), ("stn3d", "float32", None),
+                               ("gs2d_cubic", "float32", "cubic"), ("gs2d_cubic", "float16", "cubic"),
+                               ("gs2d_cubic", "float32", "nearest"),
+                               ("gs2d_cubic", "float16", "nearest"), ("gs2d_small", "float32", None),
+                               ("deform2d", "float32", None), ("deform2d", "bfloat16", None)):
+            if (name, dt, mode) == (args.workload, args.dtype, args.mode):
+                continue
+            c2 = Case(name, dt, device, mode)
+            st, _, _ = time_steps(c2, args.extra_steps, 5, flush)
+            m2 = sum(st) / len(st)
+            extra.append({"workload": workload_desc(c2), "dtype": DT_SHORT[dt],
+                          "ms_per_step": round(m2, 5), "value": round(c2.outputs / (m2 * 1e-3), 1),
+                          "unit": UNIT, "roofline": roofline_for(c2, m2, pk)})
+            del c2
+            torch.cuda.empty_cache()
+
+    cpu = oracle_sample(case) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DT_SHORT[args.dtype], "data": "synthetic (seeded PCG64; no dataset)",
+            "config": {"workload": workload_desc(case),
+                       "l2": "flushed before every step by a 512 MiB write (outside the timed interval)",
+                       "parallelism": f"replicas x{world} (independent images, no collective)"},
+            "roofline": roofline_for(case, ms, pk),
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "kernel": case.kernel_tag,
+            "src_sha": kernel_source_sha(),
+            "workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle as the reference implementation (rank 0 only)."""
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+
+    class HostCase:
+        pass
+
+    case = HostCase()
+    case.w, case.name, case.dtype = w, args.workload, args.dtype
+    case.mode = args.mode or w.mode
+    if w.kind == "affine_sample":
+        inp = wl.make_affine_sample_inputs(w)
+        case.host = {"theta": wl.as_dtype(inp["theta"], args.dtype),
+                     "X": wl.as_dtype(inp["X"], args.dtype)}
+        case.size = [int(s) for s in inp["size"]]
+    elif w.kind == "grid_sample":
+        inp = wl.make_grid_sample_inputs(w)
+        case.host = {"X": wl.as_dtype(inp["X"], args.dtype), "grid": wl.as_dtype(inp["grid"], args.dtype)}
+    else:
+        inp = wl.make_deform_inputs(w)
+        case.host = {k: wl.as_dtype(v, args.dtype) for k, v in inp.items()}
+    # the whole run stays within a few minutes: ~150 s of oracle time in all
+    per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(case, budget_s=per_step_budget / 4)
+    vals = []
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(case, budget_s=per_step_budget)
+        vals.append(last["value"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DT_SHORT[args.dtype], "data": "synthetic (seeded PCG64; no dataset)",
+        "config": {"workload": workload_desc(case),
+                   "note": "each step times the oracle on a bounded slice of whole images"},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": last["cores"],
+                         "kind": "oracle", "sample": last["sample"]},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

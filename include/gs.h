@@ -1,0 +1,181 @@
+/*
+ * gs.h -- C ABI of libgs, GB300 (sm_103a) kernels for spatial-transformer
+ * sampling: AffineGrid, GridSample, the two fused, and DeformConv.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned, dense, row-major (C-contiguous) DEVICE buffers
+ *    in the operators' layouts.  Shapes and attributes are HOST values.
+ *  - One dtype per call: theta, X, grid, W, offset, B, mask and Y all use
+ *    `dt`.  Arithmetic is fp32 (coordinates in exact fixed point, see
+ *    gs_grid_sample); half types are widened on load and rounded to nearest
+ *    even on store.
+ *  - The library allocates no memory, keeps no state between calls and never
+ *    synchronises: every call only enqueues kernels on `stream` (0 = the
+ *    legacy default stream) and returns.  Output buffers must not overlap
+ *    inputs.
+ *  - Arguments are checked on the host before anything is enqueued; a bad
+ *    argument returns its gs_status and leaves the outputs untouched.  A
+ *    failed launch returns GS_ERR_CUDA.  A tensor with a zero extent is valid
+ *    and returns GS_OK without a launch.  Nothing throws across the ABI.
+ *  - Pointers must be aligned to their element size (GS_ERR_ALIGN).
+ *  - Limits (GS_ERR_SHAPE beyond them): each spatial extent <= 2^20; each
+ *    (n, c) slab of X or Y < 2^31 elements; batch and channel counts < 2^31.
+ *  - Not safe to call concurrently from several host threads on the same
+ *    stream with overlapping outputs; otherwise thread-safe (no state).
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GS_OK = 0,
+    GS_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    GS_ERR_RANK = 2,        /* spatial rank r not supported by this entry point    */
+    GS_ERR_SHAPE = 3,       /* extents inconsistent, negative or beyond the limits */
+    GS_ERR_DTYPE = 4,       /* unknown gs_dtype                                    */
+    GS_ERR_ATTR = 5,        /* unknown mode / padding, bad kernel/stride/group ... */
+    GS_ERR_ALIGN = 6,       /* a pointer is not aligned to its element size        */
+    GS_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch        */
+    GS_ERR_TIMEOUT = 8,     /* a bounded device-side wait gave up (see gs_device_status) */
+    GS_ERR_UNSUPPORTED = 9  /* valid by the operator spec, not implemented here    */
+} gs_status;
+
+typedef enum { GS_F32 = 0, GS_F16 = 1, GS_BF16 = 2 } gs_dtype;
+
+/* GridSample - version 20, Attributes, mode.  The version-16 names "bilinear"
+ * and "bicubic" are the same modes (the Python binding maps them). */
+typedef enum { GS_LINEAR = 0, GS_NEAREST = 1, GS_CUBIC = 2 } gs_mode;
+
+/* GridSample - version 20, Attributes, padding_mode. */
+typedef enum { GS_PAD_ZEROS = 0, GS_PAD_BORDER = 1, GS_PAD_REFLECTION = 2 } gs_pad;
+
+/*
+ * gs_affine_grid -- AffineGrid (ai.onnx, since version 20): description and
+ * Inputs/Outputs.
+ *
+ *   theta  device, (N, r, r+1): the affine matrices without their implicit
+ *          last row [0 .. 0 1].
+ *   r      2 or 3.
+ *   size   host, r+2 int64: (N, C, H, W) or (N, C, D, H, W); C is unused.
+ *   align_corners  0: -1 and 1 are the outer edges of the corner pixels, the
+ *          base positions are (2i+1)/n - 1; 1: they are the corner pixel
+ *          centres, -1 + 2i/(n-1) (an axis of length 1 sits at 0).
+ *   grid   device output, (N, H, W, 2) or (N, D, H, W, 3); each vector lists
+ *          the width coordinate first.  Computed in fp64, rounded once.
+ */
+gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *size,
+                         int align_corners, void *grid, cudaStream_t stream);
+
+/*
+ * gs_grid_sample -- GridSample - version 20 (and version 22): description,
+ * Inputs, Outputs and Attributes.
+ *
+ *   X        device, (N, C, D1..Dr): values at pixel centres.
+ *   x_shape  host, r+2 int64.
+ *   r        1, 2 or 3 spatial dimensions.
+ *   grid     device, (N, D1_out..Dr_out, r); the location vector lists the
+ *            innermost axis first (x -> width, y -> height, z -> depth).
+ *   out_spatial  host, r int64: D1_out..Dr_out.
+ *   mode     linear (N-linear), nearest (ties to the even index), cubic
+ *            (N-cubic, Keys kernel with coefficient cubic_coeff_a).
+ *   pad      zeros: out-of-range taps read 0; border: clamp; reflection:
+ *            mirror at the borders until in range, then clamp.  For linear
+ *            and nearest the coordinate is padded; for cubic each tap index is.
+ *   align_corners  as in gs_affine_grid: x = (g+1)/2*(n-1) for 1,
+ *            x = ((g+1)*n - 1)/2 for 0.
+ *   cubic_coeff_a  Keys' a (the operator uses -0.75); ignored unless cubic.
+ *   Y        device output, (N, C, D1_out..Dr_out).
+ *
+ * The unnormalised coordinate is formed without rounding error (an exact
+ * product split, then 32.32 fixed point), so nearest picks the same index as
+ * exact arithmetic, ties included.
+ */
+gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const void *grid,
+                         const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                         int align_corners, float cubic_coeff_a, void *Y, cudaStream_t stream);
+
+/*
+ * gs_affine_sample -- GridSample(X, AffineGrid(theta, size)) in one kernel:
+ * the grid is generated per output position in registers and never touches
+ * memory (the spatial transformer's grid generator and sampler).
+ *
+ *   theta    device, (N, r, r+1).
+ *   size     host, r+2 int64: (N, C, out...), AffineGrid's size input; N and
+ *            C must equal X's.
+ *   X, x_shape, mode, pad, align_corners, cubic_coeff_a, Y: as gs_grid_sample,
+ *            with Y (N, C, out...).  align_corners applies to both operators.
+ *
+ * The grid is not rounded to `dt` between the two operators.  Positions are
+ * affine in the output index; the kernel evaluates that map in 64-bit fixed
+ * point (coefficients from fp64), so an identity theta reproduces X exactly.
+ */
+gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const void *X,
+                           const int64_t *x_shape, gs_dtype dt, gs_mode mode, gs_pad pad,
+                           int align_corners, float cubic_coeff_a, void *Y,
+                           cudaStream_t stream);
+
+/*
+ * DeformConv attributes.  The DeformConv page lists no Attributes section; its
+ * examples use kernel_shape, pads and offset_group.  The rest follow ONNX Conv:
+ *   kernel     (kH, kW); 0 means "take it from W".
+ *   pads       (top, left, bottom, right).
+ *   strides    (sH, sW), >= 1.     dilations (dH, dW), >= 1.
+ *   group      C and oC divisible by it.
+ *   offset_group  C divisible by it.
+ * Output extents: oH = (H + top + bottom - dH*(kH-1) - 1) / sH + 1, same for W.
+ */
+typedef struct {
+    int64_t kernel[2], pads[4], strides[2], dilations[2], group, offset_group;
+} gs_deform_attrs;
+
+/*
+ * gs_deform_conv -- DeformConv (ai.onnx, since version 22), 2-D: Inputs and
+ * Outputs.
+ *
+ *   X       device, (N, C, H, W).        x_shape host, 4 int64.
+ *   W       device, (oC, C/group, kH, kW).
+ *   oC      output channels.
+ *   offset  device, (N, offset_group*kH*kW*2, oH, oW): for offset group o and
+ *           kernel position k = kh*kW + kw, channel o*2K + 2k is the row (y)
+ *           offset and o*2K + 2k + 1 the column (x) offset, K = kH*kW.
+ *   B       device, (oC), or NULL for zeros.
+ *   mask    device, (N, offset_group*kH*kW, oH, oW), or NULL for ones.
+ *   Y       device output, (N, oC, oH, oW).
+ *
+ * Each sample is bilinear in X at (oh*sH - top + kh*dH + dy,
+ * ow*sW - left + kw*dW + dx); taps outside X read 0.  fp32 contracts with
+ * fp32 FMAs; bf16 and fp16 contract the sampled column tile on the tensor
+ * cores where the shape allows (fp32 accumulation), else with fp32 FMAs.
+ */
+gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
+                         const void *offset, const void *B, const void *mask,
+                         const gs_deform_attrs *attrs, gs_dtype dt, void *Y,
+                         cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *gs_status_str(gs_status s);
+
+/*
+ * gs_device_status -- synchronises `stream`, then reports (and clears) the
+ * library's device-side error word: GS_ERR_TIMEOUT if a bounded wait inside a
+ * kernel gave up since the last call, GS_ERR_CUDA if the stream holds a CUDA
+ * error, else GS_OK.  Kernels that give up a wait stop early and leave their
+ * output incomplete; they never trap.
+ */
+gs_status gs_device_status(cudaStream_t stream);
+
+/* Library version, "major.minor.patch" (static storage). */
+const char *gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H */

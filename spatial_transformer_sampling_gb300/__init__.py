@@ -1,1 +1,215 @@
-"""GB300-native spatial-transformer sampling (placeholder; binding added with the library)."""
+"""GB300-native spatial-transformer sampling: thin Python binding of libgs.
+
+The functions here carry the C ABI's names (include/gs.h) and only marshal
+arguments: they check that tensors are contiguous CUDA tensors of one dtype,
+allocate outputs with torch when none is given, and pass raw pointers plus the
+current torch stream to the library.  Every step of the computation runs in
+libgs's kernels.  There is no CPU fallback: if the library is missing or a
+call fails, an exception is raised.
+
+Operators (see the docstrings and include/gs.h):
+  gs_affine_grid   AffineGrid
+  gs_grid_sample   GridSample (rank 1-3; linear / nearest / cubic;
+                   zeros / border / reflection; both align_corners)
+  gs_affine_sample GridSample(X, AffineGrid(theta, size)) fused
+  gs_deform_conv   DeformConv 2-D
+"""
+import ctypes
+import os
+
+__all__ = ["gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
+           "gs_status_str", "gs_device_status", "GsError", "library_path", "load_library",
+           "EXPORTED_SYMBOLS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libgs.so")
+
+EXPORTED_SYMBOLS = ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
+                    "gs_status_str", "gs_device_status", "gs_version")
+
+MODES = {"linear": 0, "bilinear": 0, "nearest": 1, "cubic": 2, "bicubic": 2}
+PADS = {"zeros": 0, "border": 1, "reflection": 2}
+STATUS = {0: "GS_OK", 1: "GS_ERR_NULL", 2: "GS_ERR_RANK", 3: "GS_ERR_SHAPE", 4: "GS_ERR_DTYPE",
+          5: "GS_ERR_ATTR", 6: "GS_ERR_ALIGN", 7: "GS_ERR_CUDA", 8: "GS_ERR_TIMEOUT",
+          9: "GS_ERR_UNSUPPORTED"}
+
+_lib = None
+
+
+class GsError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({gs_status_str(status)})")
+
+
+class DeformAttrs(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int64 * 2), ("pads", ctypes.c_int64 * 4),
+                ("strides", ctypes.c_int64 * 2), ("dilations", ctypes.c_int64 * 2),
+                ("group", ctypes.c_int64), ("offset_group", ctypes.c_int64)]
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library(path=None):
+    """Load libgs.so (built by spatial_transformer_sampling_gb300/build.py)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libgs.so not built ({p}); run __graft_entry__.build() first")
+    L = ctypes.CDLL(p)
+    vp, i64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64)
+    ci, cf = ctypes.c_int, ctypes.c_float
+    L.gs_affine_grid.argtypes = [vp, ci, ci, i64p, ci, vp, vp]
+    L.gs_grid_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
+    L.gs_affine_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
+    L.gs_deform_conv.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
+                                 ctypes.POINTER(DeformAttrs), ci, vp, vp]
+    L.gs_status_str.argtypes = [ci]
+    L.gs_status_str.restype = ctypes.c_char_p
+    L.gs_device_status.argtypes = [vp]
+    L.gs_version.restype = ctypes.c_char_p
+    for f in ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
+              "gs_device_status"):
+        getattr(L, f).restype = ci
+    if path is None:
+        _lib = L
+    return L
+
+
+def gs_status_str(status):
+    return load_library().gs_status_str(int(status)).decode()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _check_tensors(*ts):
+    ref = next(t for t in ts if t is not None)
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("libgs takes CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("libgs takes contiguous tensors")
+        if t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError("all tensors of one call share dtype and device")
+    return ref
+
+
+def _i64(vals):
+    arr = (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+    return arr
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(t):
+    return ctypes.c_void_p(_torch().cuda.current_stream(t.device).cuda_stream)
+
+
+def _ok(status, where):
+    if status != 0:
+        raise GsError(status, where)
+
+
+def gs_affine_grid(theta, size, align_corners=0, out=None):
+    """AffineGrid: theta (N, r, r+1) -> grid (N, spatial..., r); size = (N, C, spatial...)."""
+    torch = _torch()
+    _check_tensors(theta, out)
+    size = [int(s) for s in size]
+    r = len(size) - 2
+    if out is None:
+        out = torch.empty([size[0]] + size[2:] + [r], dtype=theta.dtype, device=theta.device)
+    _ok(load_library().gs_affine_grid(_ptr(theta), _dtype_code(theta), r, _i64(size),
+                                      int(align_corners), _ptr(out), _stream(theta)),
+        "gs_affine_grid")
+    return out
+
+
+def gs_grid_sample(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
+                   cubic_coeff_a=-0.75, out=None):
+    """GridSample: X (N, C, in...), grid (N, out..., r) -> Y (N, C, out...)."""
+    torch = _torch()
+    _check_tensors(X, grid, out)
+    r = X.dim() - 2
+    out_sp = list(grid.shape[1:-1])
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
+    _ok(load_library().gs_grid_sample(_ptr(X), _i64(X.shape), r, _ptr(grid), _i64(out_sp),
+                                      _dtype_code(X), MODES[mode], PADS[padding_mode],
+                                      int(align_corners), float(cubic_coeff_a), _ptr(out),
+                                      _stream(X)), "gs_grid_sample")
+    return out
+
+
+def gs_affine_sample(theta, size, X, mode="linear", padding_mode="zeros", align_corners=0,
+                     cubic_coeff_a=-0.75, out=None):
+    """GridSample(X, AffineGrid(theta, size)) in one kernel; size = (N, C, out...)."""
+    torch = _torch()
+    _check_tensors(X, theta, out)
+    size = [int(s) for s in size]
+    r = X.dim() - 2
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + size[2:], dtype=X.dtype, device=X.device)
+    _ok(load_library().gs_affine_sample(_ptr(theta), _i64(size), r, _ptr(X), _i64(X.shape),
+                                        _dtype_code(X), MODES[mode], PADS[padding_mode],
+                                        int(align_corners), float(cubic_coeff_a), _ptr(out),
+                                        _stream(X)), "gs_affine_sample")
+    return out
+
+
+def deform_attrs(kernel_shape, pads=None, strides=None, dilations=None, group=1, offset_group=1):
+    a = DeformAttrs()
+    a.kernel[:] = [int(k) for k in kernel_shape]
+    a.pads[:] = [int(p) for p in (pads if pads is not None else (0, 0, 0, 0))]
+    a.strides[:] = [int(s) for s in (strides if strides is not None else (1, 1))]
+    a.dilations[:] = [int(d) for d in (dilations if dilations is not None else (1, 1))]
+    a.group = int(group)
+    a.offset_group = int(offset_group)
+    return a
+
+
+def deform_out_hw(H, W, a):
+    oH = (H + a.pads[0] + a.pads[2] - a.dilations[0] * (a.kernel[0] - 1) - 1) // a.strides[0] + 1
+    oW = (W + a.pads[1] + a.pads[3] - a.dilations[1] * (a.kernel[1] - 1) - 1) // a.strides[1] + 1
+    return oH, oW
+
+
+def gs_deform_conv(X, W, offset, B=None, mask=None, kernel_shape=None, pads=None, strides=None,
+                   dilations=None, group=1, offset_group=1, out=None):
+    """DeformConv 2-D: X (N,C,H,W), W (oC,C/group,kH,kW), offset (N,og*kH*kW*2,oH,oW)."""
+    torch = _torch()
+    _check_tensors(X, W, offset, B, mask, out)
+    a = deform_attrs(kernel_shape if kernel_shape is not None else W.shape[2:], pads, strides,
+                     dilations, group, offset_group)
+    oH, oW = deform_out_hw(X.shape[2], X.shape[3], a)
+    if out is None:
+        out = torch.empty((X.shape[0], W.shape[0], oH, oW), dtype=X.dtype, device=X.device)
+    _ok(load_library().gs_deform_conv(_ptr(X), _i64(X.shape), _ptr(W), int(W.shape[0]),
+                                      _ptr(offset), _ptr(B), _ptr(mask), ctypes.byref(a),
+                                      _dtype_code(X), _ptr(out), _stream(X)), "gs_deform_conv")
+    return out
+
+
+def gs_device_status(device=None):
+    """Synchronise the current stream and report the library's device error word."""
+    torch = _torch()
+    s = torch.cuda.current_stream(device).cuda_stream
+    return load_library().gs_device_status(ctypes.c_void_p(s))

@@ -1,0 +1,220 @@
+// gs_api.cu -- the C ABI of libgs (declared in include/gs.h): host-side
+// argument checks, then dispatch to the per-dtype launchers.  Nothing here
+// allocates, synchronises (except gs_device_status) or throws.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "../../include/gs.h"
+#include "gs_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxExtent = int64_t(1) << 20;
+constexpr int64_t kMaxSlab = (int64_t(1) << 31) - 1;
+
+size_t elem_size(gs_dtype dt) { return dt == GS_F32 ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == GS_F32 || dt == GS_F16 || dt == GS_BF16; }
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+template <typename F>
+gs_status dispatch(gs_dtype dt, F &&f) {
+    cudaError_t e;
+    switch (dt) {
+        case GS_F32: e = f(float()); break;
+        case GS_F16: e = f(__half()); break;
+        default: e = f(__nv_bfloat16()); break;
+    }
+    return e == cudaSuccess ? GS_OK : GS_ERR_CUDA;
+}
+
+// Spatial extents: all >= 0, each <= 2^20, product (returned) < 2^31.
+gs_status check_spatial(const int64_t *ext, int r, int64_t *prod, bool *empty) {
+    int64_t p = 1;
+    *empty = false;
+    for (int d = 0; d < r; ++d) {
+        if (ext[d] < 0 || ext[d] > kMaxExtent) return GS_ERR_SHAPE;
+        if (ext[d] == 0) *empty = true;
+        p *= ext[d];
+        if (p > kMaxSlab) return GS_ERR_SHAPE;
+    }
+    *prod = p;
+    return GS_OK;
+}
+
+bool nc_ok(int64_t N, int64_t C) { return N >= 0 && C >= 0 && N <= kMaxSlab && C <= kMaxSlab; }
+
+// Shared checks of gs_grid_sample and gs_affine_sample.
+gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64_t *out_sp,
+                       gs_dtype dt, gs_mode mode, gs_pad pad, int ac, float a, const void *Y,
+                       gs::SampleArgs *args, bool *skip) {
+    if (!x_shape || !out_sp) return GS_ERR_NULL;
+    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
+    if ((int)mode < GS_LINEAR || (int)mode > GS_CUBIC) return GS_ERR_ATTR;
+    if ((int)pad < GS_PAD_ZEROS || (int)pad > GS_PAD_REFLECTION) return GS_ERR_ATTR;
+    if (ac != 0 && ac != 1) return GS_ERR_ATTR;
+    if (mode == GS_CUBIC && !isfinite(a)) return GS_ERR_ATTR;
+    const int64_t N = x_shape[0], C = x_shape[1];
+    if (!nc_ok(N, C)) return GS_ERR_SHAPE;
+    int64_t in_plane, out_plane;
+    bool in_empty, out_empty;
+    gs_status st = check_spatial(x_shape + 2, r, &in_plane, &in_empty);
+    if (st != GS_OK) return st;
+    st = check_spatial(out_sp, r, &out_plane, &out_empty);
+    if (st != GS_OK) return st;
+    *skip = out_empty || N == 0 || C == 0;
+    if (*skip) return GS_OK;
+    if (in_empty) return GS_ERR_SHAPE;   // nothing to sample from
+    if (!X || !Y) return GS_ERR_NULL;
+    if (!aligned(X, elem_size(dt)) || !aligned(Y, elem_size(dt))) return GS_ERR_ALIGN;
+    const int64_t tiles = (out_plane + gs::kSampleThreads - 1) / gs::kSampleThreads;
+    if (N * tiles > kMaxSlab) return GS_ERR_SHAPE;
+    args->N = (int)N;
+    args->C = (int)C;
+    for (int d = 0; d < 3; ++d) {
+        args->in[d] = d < r ? (int)x_shape[2 + d] : 1;
+        args->out[d] = d < r ? (int)out_sp[d] : 1;
+    }
+    args->in_plane = in_plane;
+    args->out_plane = out_plane;
+    args->tiles = (int)tiles;
+    args->pad = (int)pad;
+    args->ac = ac;
+    args->a = a;
+    return GS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *size,
+                         int align_corners, void *grid, cudaStream_t stream) {
+    if (!size) return GS_ERR_NULL;
+    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
+    if (r != 2 && r != 3) return GS_ERR_RANK;
+    if (align_corners != 0 && align_corners != 1) return GS_ERR_ATTR;
+    const int64_t N = size[0];
+    if (!nc_ok(N, size[1])) return GS_ERR_SHAPE;
+    int64_t plane;
+    bool empty;
+    gs_status st = check_spatial(size + 2, r, &plane, &empty);
+    if (st != GS_OK) return st;
+    if (empty || N == 0) return GS_OK;
+    if (!theta || !grid) return GS_ERR_NULL;
+    if (!aligned(theta, elem_size(dt)) || !aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
+    if ((N * plane + 255) / 256 > kMaxSlab) return GS_ERR_SHAPE;
+    gs::AffineGridArgs a;
+    a.N = (int)N;
+    for (int d = 0; d < 3; ++d) a.out[d] = d < r ? (int)size[2 + d] : 1;
+    a.out_plane = plane;
+    a.ac = align_corners;
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_affine_grid<decltype(tag)>(theta, grid, a, r, stream);
+    });
+}
+
+gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const void *grid,
+                         const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                         int align_corners, float cubic_coeff_a, void *Y, cudaStream_t stream) {
+    if (r < 1 || r > 3) return GS_ERR_RANK;
+    gs::SampleArgs args;
+    bool skip = false;
+    gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,
+                                cubic_coeff_a, Y, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    if (!grid) return GS_ERR_NULL;
+    if (!aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, stream);
+    });
+}
+
+gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const void *X,
+                           const int64_t *x_shape, gs_dtype dt, gs_mode mode, gs_pad pad,
+                           int align_corners, float cubic_coeff_a, void *Y,
+                           cudaStream_t stream) {
+    if (r != 2 && r != 3) return GS_ERR_RANK;
+    if (!size || !x_shape) return GS_ERR_NULL;
+    if (size[0] != x_shape[0] || size[1] != x_shape[1]) return GS_ERR_SHAPE;
+    gs::SampleArgs args;
+    bool skip = false;
+    gs_status st = check_sample(X, x_shape, r, size + 2, dt, mode, pad, align_corners,
+                                cubic_coeff_a, Y, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    if (!theta) return GS_ERR_NULL;
+    if (!aligned(theta, elem_size(dt))) return GS_ERR_ALIGN;
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_sample<decltype(tag)>(X, theta, Y, args, r, (int)mode, true, stream);
+    });
+}
+
+gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
+                         const void *offset, const void *B, const void *mask,
+                         const gs_deform_attrs *at, gs_dtype dt, void *Y, cudaStream_t stream) {
+    if (!x_shape || !at) return GS_ERR_NULL;
+    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
+    const int64_t N = x_shape[0], C = x_shape[1], H = x_shape[2], Wd = x_shape[3];
+    if (!nc_ok(N, C) || oC < 0 || oC > kMaxSlab) return GS_ERR_SHAPE;
+    if (H < 0 || Wd < 0 || H > kMaxExtent || Wd > kMaxExtent || H * Wd > kMaxSlab)
+        return GS_ERR_SHAPE;
+    for (int i = 0; i < 2; ++i) {
+        if (at->kernel[i] < 1 || at->kernel[i] > 64) return GS_ERR_ATTR;
+        if (at->strides[i] < 1 || at->dilations[i] < 1) return GS_ERR_ATTR;
+        if (at->strides[i] > kMaxExtent || at->dilations[i] > kMaxExtent) return GS_ERR_ATTR;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (at->pads[i] < 0 || at->pads[i] > kMaxExtent) return GS_ERR_ATTR;
+    if (at->group < 1 || at->offset_group < 1) return GS_ERR_ATTR;
+    if (C % at->group || oC % at->group || C % at->offset_group) return GS_ERR_ATTR;
+    const int64_t kH = at->kernel[0], kW = at->kernel[1];
+    const int64_t oH = (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1) / at->strides[0] + 1;
+    const int64_t oW = (Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1) / at->strides[1] + 1;
+    if (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1 < 0 ||
+        Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1 < 0)
+        return GS_ERR_SHAPE;
+    if (oH * oW > kMaxSlab) return GS_ERR_SHAPE;
+    if (N == 0 || oC == 0 || oH == 0 || oW == 0) return GS_OK;
+    if (C == 0 || H == 0 || Wd == 0) return GS_ERR_SHAPE;
+    if (!X || !W || !offset || !Y) return GS_ERR_NULL;
+    const size_t es = elem_size(dt);
+    if (!aligned(X, es) || !aligned(W, es) || !aligned(offset, es) || !aligned(Y, es) ||
+        (B && !aligned(B, es)) || (mask && !aligned(mask, es)))
+        return GS_ERR_ALIGN;
+    gs::DeformArgs a;
+    a.N = (int)N; a.C = (int)C; a.H = (int)H; a.W = (int)Wd; a.oC = (int)oC;
+    a.oH = (int)oH; a.oW = (int)oW; a.kH = (int)kH; a.kW = (int)kW;
+    a.pad_t = (int)at->pads[0]; a.pad_l = (int)at->pads[1];
+    a.sH = (int)at->strides[0]; a.sW = (int)at->strides[1];
+    a.dH = (int)at->dilations[0]; a.dW = (int)at->dilations[1];
+    a.group = (int)at->group; a.offset_group = (int)at->offset_group;
+    a.has_bias = B != nullptr; a.has_mask = mask != nullptr;
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_deform<decltype(tag)>(X, W, offset, B, mask, Y, a, stream);
+    });
+}
+
+const char *gs_status_str(gs_status s) {
+    switch (s) {
+        case GS_OK: return "ok";
+        case GS_ERR_NULL: return "null pointer";
+        case GS_ERR_RANK: return "unsupported spatial rank";
+        case GS_ERR_SHAPE: return "bad shape";
+        case GS_ERR_DTYPE: return "bad dtype";
+        case GS_ERR_ATTR: return "bad attribute";
+        case GS_ERR_ALIGN: return "misaligned pointer";
+        case GS_ERR_CUDA: return "CUDA error";
+        case GS_ERR_TIMEOUT: return "device-side wait timed out";
+        case GS_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+gs_status gs_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GS_ERR_CUDA;
+    return GS_OK;
+}
+
+const char *gs_version(void) { return "0.1.0"; }
+
+}  // extern "C"

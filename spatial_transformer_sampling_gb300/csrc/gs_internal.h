@@ -1,0 +1,53 @@
+// gs_internal.h -- host-side interface between the C ABI (gs_api.cu) and the
+// per-dtype kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gs {
+
+constexpr int kSampleThreads = 256;
+
+struct Axis;   // gs_common.cuh
+
+// Arguments of the sampling kernels (GridSample and the fused affine path).
+struct SampleArgs {
+    int N, C;
+    int in[3];           // input spatial extents, outermost first (1 when unused)
+    int out[3];          // output spatial extents, outermost first
+    int64_t in_plane;    // product of in[]
+    int64_t out_plane;   // product of out[]
+    int tiles;           // blocks per image: ceil(out_plane / kSampleThreads)
+    int pad, ac;
+    float a;             // Keys coefficient
+};
+
+// Arguments of the standalone AffineGrid kernel.
+struct AffineGridArgs {
+    int N;
+    int out[3];
+    int64_t out_plane;
+    int ac;
+};
+
+// Arguments of DeformConv.
+struct DeformArgs {
+    int N, C, H, W, oC, oH, oW;
+    int kH, kW, pad_t, pad_l, sH, sW, dH, dW, group, offset_group;
+    int has_bias, has_mask;
+};
+
+// Per-dtype launchers; T is float, __half or __nv_bfloat16.  Each enqueues on
+// `s` and returns the launch error (cudaSuccess when fine).
+template <typename T>
+cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
+                          int mode, bool affine, cudaStream_t s);
+template <typename T>
+cudaError_t launch_affine_grid(const void *theta, void *grid, const AffineGridArgs &args, int r,
+                               cudaStream_t s);
+template <typename T>
+cudaError_t launch_deform(const void *X, const void *W, const void *offset, const void *B,
+                          const void *mask, void *Y, const DeformArgs &args, cudaStream_t s);
+
+}  // namespace gs

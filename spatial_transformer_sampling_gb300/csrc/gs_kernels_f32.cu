@@ -1,0 +1,13 @@
+// gs_kernels_f32.cu -- float instantiations of the libgs kernels (one
+// translation unit per dtype so the build compiles them in parallel).
+#include "gs_deform.cuh"
+#include "gs_sample.cuh"
+
+namespace gs {
+template cudaError_t launch_sample<float>(const void *, const void *, void *, const SampleArgs &,
+                                          int, int, bool, cudaStream_t);
+template cudaError_t launch_affine_grid<float>(const void *, void *, const AffineGridArgs &, int,
+                                               cudaStream_t);
+template cudaError_t launch_deform<float>(const void *, const void *, const void *, const void *,
+                                          const void *, void *, const DeformArgs &, cudaStream_t);
+}  // namespace gs

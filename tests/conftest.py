@@ -54,3 +54,35 @@ def oracle_mod():
     import oracle
     oracle.lib()
     return oracle
+
+
+# Parity bars: fp32 |y - ref| <= 1e-6 + 1e-5 |ref|; fp16/bf16 <= 1e-2 + 1e-2 |ref|.
+TOL = {"float32": (1e-6, 1e-5), "float16": (1e-2, 1e-2), "bfloat16": (1e-2, 1e-2)}
+
+
+def assert_parity(got, ref, dtype, what=""):
+    """Element-wise comparison of a CUDA result (torch tensor) with oracle values."""
+    import torch
+    g = got.detach().to("cpu").to(torch.float64).numpy() if hasattr(got, "detach") else got
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    atol, rtol = TOL[dtype]
+    err = np.abs(g - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err, -1)), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside {atol} + {rtol}|ref| "
+                             f"(worst at {i}: got {g[i]!r}, ref {ref[i]!r})")
+
+
+@pytest.fixture(scope="session")
+def gs_cuda():
+    """The CUDA library, built for this machine; fails loudly when it cannot load."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without a CUDA device")
+    from spatial_transformer_sampling_gb300 import build as gsbuild
+    gsbuild.build()
+    import spatial_transformer_sampling_gb300 as gs
+    gs.load_library()
+    return gs

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry point
+include/gs.h declares, and rejects bad arguments on the host (before any
+CUDA call, so these run on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import spatial_transformer_sampling_gb300 as gs
+from spatial_transformer_sampling_gb300 import build as gsbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gs.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    gsbuild.build()
+    return gs.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gs_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(gs.EXPORTED_SYMBOLS) <= set(declared_functions())
+
+
+def test_version_and_status_strings(L):
+    assert L.gs_version().decode().count(".") == 2
+    assert gs.gs_status_str(0) == "ok"
+    assert "shape" in gs.gs_status_str(3)
+
+
+def _i64(v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+FAKE = 0x10000   # a non-null, aligned pointer value; never dereferenced on these paths
+
+
+def _gsample(L, x_shape, out, r=2, dt=0, mode=0, pad=0, ac=0, a=-0.75, X=FAKE, grid=FAKE, Y=FAKE):
+    return L.gs_grid_sample(X, _i64(x_shape), r, grid, _i64(out), dt, mode, pad, ac, a, Y, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(mode=3), 5), (dict(pad=-1), 5), (dict(ac=2), 5), (dict(dt=9), 4),
+    (dict(r=4, x_shape=[1, 1, 2, 2, 2, 2], out=[2, 2, 2, 2]), 2), (dict(r=0), 2),
+    (dict(X=None), 1), (dict(Y=None), 1), (dict(grid=None), 1),
+    (dict(X=FAKE + 2), 6), (dict(dt=1, Y=FAKE + 1), 6),
+    (dict(x_shape=[1, 1, 1 << 21, 2]), 3), (dict(x_shape=[1, 1, -1, 2]), 3),
+    (dict(x_shape=[1, 1, 1 << 16, 1 << 16]), 3), (dict(x_shape=[1, 1, 0, 4]), 3),
+    (dict(mode=2, a=float("nan")), 5),
+])
+def test_grid_sample_rejects_bad_arguments(L, kwargs, status):
+    args = dict(x_shape=[2, 3, 4, 5], out=[3, 3])
+    args.update(kwargs)
+    assert _gsample(L, **args) == status
+
+
+@pytest.mark.parametrize("x_shape,out", [([0, 3, 4, 5], [3, 3]), ([2, 0, 4, 5], [3, 3]),
+                                         ([2, 3, 4, 5], [0, 3])])
+def test_empty_tensors_return_ok_without_a_launch(L, x_shape, out):
+    assert _gsample(L, x_shape, out, X=None, grid=None, Y=None) == 0
+
+
+def test_affine_sample_checks(L):
+    f = L.gs_affine_sample
+    assert f(FAKE, _i64([2, 3, 4, 4]), 1, FAKE, _i64([2, 3, 4]), 0, 0, 0, 0, -0.75, FAKE, None) == 2
+    assert f(FAKE, _i64([2, 4, 4, 4]), 2, FAKE, _i64([2, 3, 4, 4]), 0, 0, 0, 0, -0.75, FAKE, None) == 3
+    assert f(None, _i64([2, 3, 4, 4]), 2, FAKE, _i64([2, 3, 4, 4]), 0, 0, 0, 0, -0.75, FAKE, None) == 1
+    assert f(FAKE, _i64([0, 3, 4, 4]), 2, None, _i64([0, 3, 4, 4]), 0, 0, 0, 0, -0.75, None, None) == 0
+
+
+def test_affine_grid_checks(L):
+    f = L.gs_affine_grid
+    assert f(FAKE, 0, 1, _i64([1, 1, 4]), 0, FAKE, None) == 2
+    assert f(FAKE, 0, 2, _i64([1, 1, 4, 4]), 3, FAKE, None) == 5
+    assert f(FAKE, 5, 2, _i64([1, 1, 4, 4]), 0, FAKE, None) == 4
+    assert f(None, 0, 2, _i64([1, 1, 4, 4]), 0, FAKE, None) == 1
+    assert f(None, 0, 2, _i64([0, 1, 4, 4]), 0, None, None) == 0
+
+
+def _deform(L, x_shape=(1, 4, 8, 8), oC=4, kernel=(3, 3), pads=(1, 1, 1, 1), strides=(1, 1),
+            dil=(1, 1), group=1, og=1, X=FAKE):
+    a = gs.deform_attrs(kernel, pads, strides, dil, group, og)
+    return L.gs_deform_conv(X, _i64(list(x_shape)), FAKE, oC, FAKE, None, None, ctypes.byref(a), 0,
+                            FAKE, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(group=3), 5), (dict(og=3), 5), (dict(oC=6, group=4), 5), (dict(kernel=(0, 3)), 5),
+    (dict(strides=(0, 1)), 5), (dict(dil=(1, 0)), 5), (dict(pads=(-1, 0, 0, 0)), 5),
+    (dict(x_shape=(1, 4, 2, 2), pads=(0, 0, 0, 0)), 3), (dict(X=None), 1),
+])
+def test_deform_conv_rejects_bad_arguments(L, kwargs, status):
+    assert _deform(L, **kwargs) == status
+
+
+def test_deform_conv_null_attrs(L):
+    assert L.gs_deform_conv(FAKE, _i64([1, 1, 4, 4]), FAKE, 1, FAKE, None, None, None, 0, FAKE,
+                            None) == 1

@@ -1,0 +1,90 @@
+"""DeformConv on the GPU against the oracle, element by element on seeded inputs,
+plus the page's worked examples and the full-size workload on sampled outputs."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_parity, fixture_array, fixture_names, load_fixture, page_close
+from spatial_transformer_sampling_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def exact(t):
+    return wl.widened(t)
+
+
+@pytest.mark.parametrize("name", fixture_names("deformconv__"))
+def test_page_examples_deform_conv(gs_cuda, oracle_mod, name):
+    fx = load_fixture(name)
+    a = fx["attributes"]
+    ins = {k: fixture_array(v) for k, v in fx["inputs"].items()}
+    kw = dict(kernel_shape=a.get("kernel_shape"), pads=a.get("pads"),
+              offset_group=a.get("offset_group", 1))
+    cu = {k: wl.as_dtype(v, "float32").cuda() for k, v in ins.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu.get("B"), cu.get("mask"), **kw)
+    ref = oracle_mod.deform_conv(ins["X"], ins["W"], ins["offset"], ins.get("B"), ins.get("mask"),
+                                 **kw)
+    assert_parity(Y, ref, "float32", fx["citation"])
+    assert page_close(exact(Y), fixture_array(fx["outputs"]["Y"])).all(), fx["citation"]
+
+
+CASES = [
+    # N, C, H, W, oC, kernel, pads, strides, dilations, group, og, bias, mask
+    (2, 8, 13, 11, 6, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True),
+    (1, 6, 9, 14, 4, (3, 2), (0, 1, 2, 0), (2, 1), (1, 2), 2, 1, False, True),
+    (2, 8, 10, 10, 8, (2, 2), (1, 0, 0, 1), (1, 2), (2, 1), 1, 2, True, False),
+    (1, 12, 11, 9, 6, (3, 3), (2, 2, 2, 2), (2, 2), (2, 2), 3, 4, True, True),
+    (1, 40, 9, 17, 70, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True),   # 2 oc blocks, ragged chunks
+    (1, 64, 12, 12, 16, (1, 1), (0, 0, 0, 0), (1, 1), (1, 1), 1, 64, False, True),   # 1 channel per offset group
+    (3, 4, 5, 31, 3, (5, 3), (2, 1, 2, 1), (1, 3), (1, 1), 1, 1, True, False),
+]
+
+
+@pytest.mark.parametrize("case,dtype", list(itertools.product(range(len(CASES)),
+                                                              ["float32", "float16", "bfloat16"])))
+def test_deform_conv_cases(gs_cuda, oracle_mod, case, dtype):
+    N, C, H, W, oC, k, p, s, d, grp, og, has_b, has_m = CASES[case]
+    g = wl.rng(300 + case)
+    oH = (H + p[0] + p[2] - d[0] * (k[0] - 1) - 1) // s[0] + 1
+    oW = (W + p[1] + p[3] - d[1] * (k[1] - 1) - 1) // s[1] + 1
+    K = k[0] * k[1]
+    host = {
+        "X": wl.as_dtype(g.normal(size=(N, C, H, W)), dtype),
+        "W": wl.as_dtype(g.normal(0, 0.3, size=(oC, C // grp) + k), dtype),
+        "offset": wl.as_dtype(g.normal(0, 1.5, size=(N, og * K * 2, oH, oW)), dtype),
+        "B": wl.as_dtype(g.normal(size=(oC,)), dtype) if has_b else None,
+        "mask": wl.as_dtype(g.uniform(0, 1, size=(N, og * K, oH, oW)), dtype) if has_m else None,
+    }
+    kw = dict(kernel_shape=k, pads=p, strides=s, dilations=d, group=grp, offset_group=og)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Y, ref, dtype, f"deform case {case} {dtype}")
+
+
+def test_deform_conv_zero_batch_and_channels(gs_cuda):
+    X = torch.zeros((0, 4, 8, 8), device="cuda")
+    W = torch.zeros((5, 4, 3, 3), device="cuda")
+    off = torch.zeros((0, 18, 8, 8), device="cuda")
+    assert gs_cuda.gs_deform_conv(X, W, off, pads=(1, 1, 1, 1)).shape == (0, 5, 8, 8)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_full_size_deform2d(gs_cuda, oracle_mod, dtype):
+    w = wl.WORKLOADS["deform2d"]
+    inp = wl.make_deform_inputs(w)
+    host = {k: wl.as_dtype(v, dtype) for k, v in inp.items()}
+    cu = {k: v.cuda() for k, v in host.items()}
+    kw = dict(kernel_shape=w.kernel, pads=w.pads, strides=w.strides, dilations=w.dilations,
+              group=w.group, offset_group=w.offset_group)
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    torch.cuda.synchronize()
+    g = wl.rng(5)
+    idx = np.unique(np.concatenate([g.integers(0, Y.numel(), 20000), [0, Y.numel() - 1]]))
+    ref = oracle_mod.deform_conv_at(exact(host["X"]), exact(host["W"]), exact(host["offset"]), idx,
+                                    exact(host["B"]), exact(host["mask"]), **kw)
+    assert_parity(Y.reshape(-1)[torch.from_numpy(idx).cuda()], ref, dtype, "deform2d sampled")
