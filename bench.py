@@ -7,8 +7,10 @@ A step is one pass of the hot path over one batch: by default the fused
 AffineGrid+GridSample 2-D workload "stn2d" -- theta (64,2,3) = identity +
 N(0,0.1), X (64,32,128,128) ~ N(0,1) fp32, output 128x128, linear, border,
 align_corners=1 -- one gs_affine_sample call.  Inputs are seeded synthetic
-data resident in HBM before the timed region; L2 is flushed (a 512 MiB write)
-before every timed step, outside the step's CUDA-event interval.  Time is
+data resident in HBM before the timed region; L2 is flushed before every timed
+step, outside the step's CUDA-event interval: a 512 MiB buffer is written and
+then read, so L2 holds only clean, unrelated lines when the step starts (no
+write-back of the flush is charged to the step).  Time is
 taken with CUDA events on the stream the kernel runs on; the timed region is
 bracketed by barrier + synchronize, and the max over ranks is reported.
 
@@ -226,12 +228,18 @@ class Case:
                                       offset_group=w.offset_group, out=out)
 
 
+def flush_l2(buf):
+    """Write then read a buffer larger than L2 (leaves L2 clean and cold for the step)."""
+    buf.zero_()
+    return buf.amax()
+
+
 def time_steps(case, steps, warmup, flush, barrier=None):
     """Per-step CUDA-event durations (ms) of the hot path, L2 flushed before each step."""
     import torch
     stream = torch.cuda.current_stream(case.device)
     for _ in range(warmup):
-        flush.zero_()
+        flush_l2(flush)
         case.run()
     torch.cuda.synchronize(case.device)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -241,7 +249,7 @@ def time_steps(case, steps, warmup, flush, barrier=None):
     torch.cuda.synchronize(case.device)
     t0 = time.time()
     for i in range(steps):
-        flush.zero_()
+        flush_l2(flush)
         starts[i].record(stream)
         case.run()
         ends[i].record(stream)
@@ -420,7 +428,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DT_SHORT[args.dtype], "data": "synthetic (seeded PCG64; no dataset)",
             "config": {"workload": workload_desc(case),
-                       "l2": "flushed before every step by a 512 MiB write (outside the timed interval)",
+                       "l2": "flushed before every step: 512 MiB written then read (outside the timed interval)",
                        "parallelism": f"replicas x{world} (independent images, no collective)"},
             "roofline": roofline_for(case, ms, pk),
             "cpu_baseline": cpu,

@@ -8,7 +8,25 @@
 #include "../../include/gs.h"
 #include "gs_internal.h"
 
+// Device error word: kernels whose bounded waits give up record it here;
+// gs_device_status reads and clears it.
+__device__ unsigned g_gs_error_word = 0;
+
 namespace {
+
+// Device address of g_gs_error_word on the current device (looked up once per
+// device; a host-side symbol is not a device address).
+unsigned *error_word() {
+    static unsigned *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gs_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = (unsigned *)p;
+    }
+    return cache[dev];
+}
 
 constexpr int64_t kMaxExtent = int64_t(1) << 20;
 constexpr int64_t kMaxSlab = (int64_t(1) << 31) - 1;
@@ -81,6 +99,7 @@ gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64
     args->pad = (int)pad;
     args->ac = ac;
     args->a = a;
+    args->err = nullptr;
     return GS_OK;
 }
 
@@ -125,6 +144,7 @@ gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const voi
     if (st != GS_OK || skip) return st;
     if (!grid) return GS_ERR_NULL;
     if (!aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
+    args.err = error_word();
     return dispatch(dt, [&](auto tag) {
         return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, stream);
     });
@@ -144,6 +164,7 @@ gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const 
     if (st != GS_OK || skip) return st;
     if (!theta) return GS_ERR_NULL;
     if (!aligned(theta, elem_size(dt))) return GS_ERR_ALIGN;
+    args.err = error_word();
     return dispatch(dt, [&](auto tag) {
         return gs::launch_sample<decltype(tag)>(X, theta, Y, args, r, (int)mode, true, stream);
     });
@@ -212,6 +233,13 @@ const char *gs_status_str(gs_status s) {
 
 gs_status gs_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return GS_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_gs_error_word, sizeof(word)) != cudaSuccess) return GS_ERR_CUDA;
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_gs_error_word, &zero, sizeof(zero)) != cudaSuccess) return GS_ERR_CUDA;
+        return GS_ERR_TIMEOUT;
+    }
     return GS_OK;
 }
 

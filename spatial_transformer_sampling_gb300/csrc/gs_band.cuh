@@ -1,0 +1,331 @@
+// gs_band.cuh -- fused AffineGrid+GridSample, 2-D: the streamed band kernel.
+//
+// A block owns one image and a band of `th` consecutive output rows (full
+// width).  Under an affine map the input rows a band reads form one
+// contiguous range [r0, r0+rows) of every channel plane: the row position is
+// affine in the output index, so its extremes over the band sit at the
+// band's corners.  One elected thread streams that range channel by channel
+// into a ring of shared-memory stages with bulk async copies (one contiguous
+// cp.async.bulk per channel, completion counted on an mbarrier), and every
+// thread interpolates its positions from shared memory.  DRAM sees long
+// contiguous reads instead of short gathers, and the taps are plain
+// shared-memory loads instead of multi-sector L1 requests.
+//
+// Taps are flattened once per position into byte offsets inside a stage plus
+// combined weights.  Each stage ends with a 16-byte zero pad: a tap outside X
+// (zeros padding) points at it, so it reads exactly 0 with no branch or
+// select.  The ring is split into as many stages as the band's row range
+// allows (up to 16).  A band whose rows do not fit two stages (strong
+// zoom-out, large rotation, reflection of far-out positions) or whose map
+// needs fp64 gathers from global memory instead, with the same taps.
+#pragma once
+
+#include "gs_ptx.cuh"
+
+namespace gs {
+
+constexpr int kBandThreads = 256;
+constexpr int kBandPPT = 4;          // output positions per thread: th * Wo <= 1024
+constexpr int kBandMaxStages = 16;
+constexpr int kBandMinStages = 2;
+constexpr int kBandZeroPad = 16;     // bytes of zeros after each stage's rows
+
+// Blocks per SM the register allocation must allow: 4 for linear and nearest
+// (a 64-register budget, which their taps fit); cubic's 16 taps per position
+// need more registers than that, so it runs fewer, larger blocks.
+template <int MODE> struct BandMinBlocks { static constexpr int value = 4; };
+template <> struct BandMinBlocks<MODE_CUBIC> { static constexpr int value = 1; };
+
+struct BandParams {
+    int th;            // output rows per band
+    int bands;         // bands per image
+    int ring_bytes;    // shared-memory ring, split into stages per band
+};
+
+// Shared-memory load at a 32-bit shared address (volatile: never moved across
+// the stage waits and barriers).
+template <typename T> __device__ __forceinline__ float lds_at(uint32_t addr);
+template <> __device__ __forceinline__ float lds_at<float>(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+template <> __device__ __forceinline__ float lds_at<__half>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __half2float(__ushort_as_half(v));
+}
+template <> __device__ __forceinline__ float lds_at<__nv_bfloat16>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __uint_as_float((uint32_t)v << 16);
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kBandThreads, BandMinBlocks<MODE>::value)
+band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict__ Y,
+            const SampleParams P, const BandParams B) {
+    constexpr int K = TapCount<MODE>::K;
+    constexpr int NT = K * K;
+    extern __shared__ __align__(128) unsigned char band_smem[];
+    __shared__ __align__(8) uint64_t full[kBandMaxStages];
+    __shared__ AffineMap s_map;
+    __shared__ int s_r0, s_rows, s_stages, s_abort;
+
+    const SampleArgs &a = P.a;
+    const int n = blockIdx.x / B.bands;
+    const int band = blockIdx.x - n * B.bands;
+    const int Ho = a.out[0], Wo = a.out[1], Hi = a.in[0], Wi = a.in[1];
+    const int h0 = band * B.th;
+    const int hn = min(B.th, Ho - h0);
+    const int npos = hn * Wo;
+    const int tid = threadIdx.x;
+
+    if (tid < 32) build_affine_map_warp<T, 2>(theta + (int64_t)n * 6, P, s_map);
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < kBandMaxStages; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        // input row range of the band, from the four corners
+        int stages = 0, lo = 0, hi = 0;
+        if (!s_map.wide) {
+            int64_t ymin = INT64_MAX, ymax = INT64_MIN;
+            for (int ci = 0; ci < 4; ++ci) {
+                const int h = (ci & 1) ? h0 + hn - 1 : h0;
+                const int w = (ci & 2) ? Wo - 1 : 0;
+                const int64_t y = (s_map.cst_q[0] + s_map.coef_q[0][0] * h +
+                                   s_map.coef_q[0][1] * w) >> 8;
+                ymin = y < ymin ? y : ymin;
+                ymax = y > ymax ? y : ymax;
+            }
+            lo = (int)(ymin >> 32) - (MODE == MODE_CUBIC ? 1 : 0);
+            hi = (int)(ymax >> 32) + (MODE == MODE_CUBIC ? 2 : 1);
+            if (a.pad == PAD_REFLECTION && (lo < 0 || hi > Hi - 1)) {
+                lo = 0;   // folded positions can land anywhere: take the plane
+                hi = Hi - 1;
+            }
+            // Border padding moves taps onto rows 0 and Hi-1, zeros padding
+            // masks taps outside; either way clamping both ends into range
+            // keeps every row a tap reads.
+            lo = min(max(lo, 0), Hi - 1);
+            hi = min(max(hi, 0), Hi - 1);
+            const int64_t stage = (int64_t)(hi - lo + 1) * Wi * (int64_t)sizeof(T) + kBandZeroPad;
+            stages = (int)min((int64_t)kBandMaxStages, (int64_t)B.ring_bytes / stage);
+            if (stages < kBandMinStages) stages = 0;
+        }
+        s_r0 = lo;
+        s_rows = hi - lo + 1;
+        s_stages = stages;
+        s_abort = 0;
+    }
+    __syncthreads();
+    const int S = s_stages;   // 0: gather from global
+    const int r0 = s_r0, rows = s_rows;
+    const uint32_t data_bytes = (uint32_t)rows * (uint32_t)Wi * (uint32_t)sizeof(T);
+    const uint32_t stage_bytes = data_bytes + kBandZeroPad;
+
+    // flattened taps of this thread's positions (tid, tid+256, ...: each
+    // channel's stores are whole lines per warp)
+    uint32_t off[kBandPPT][NT];
+    float wt[kBandPPT][NT];
+    uint32_t okm[kBandPPT];
+    int pos[kBandPPT];
+#pragma unroll
+    for (int j = 0; j < kBandPPT; ++j) {
+        const int p = tid + j * kBandThreads;
+        pos[j] = p < npos ? p : -1;
+        const int pp = p < npos ? p : 0;
+        const int h = h0 + pp / Wo, w = pp - (pp / Wo) * Wo;
+        int64_t yq, xq;
+        if (!s_map.wide) {
+            yq = (s_map.cst_q[0] + s_map.coef_q[0][0] * h + s_map.coef_q[0][1] * w) >> 8;
+            xq = (s_map.cst_q[1] + s_map.coef_q[1][0] * h + s_map.coef_q[1][1] * w) >> 8;
+        } else {
+            yq = pos_to_q(s_map.cst[0] + s_map.coef[0][0] * h + s_map.coef[0][1] * w, P.ax[0], a.pad);
+            xq = pos_to_q(s_map.cst[1] + s_map.coef[1][0] * h + s_map.coef[1][1] * w, P.ax[1], a.pad);
+        }
+        AxisTaps<MODE> ty, tx;
+        make_taps<MODE>(yq, P.ax[0], a.pad, a.ac, a.a, ty);
+        make_taps<MODE>(xq, P.ax[1], a.pad, a.ac, a.a, tx);
+        okm[j] = 0;
+#pragma unroll
+        for (int ky = 0; ky < K; ++ky) {
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) {
+                const int t = ky * K + kx;
+                const bool ok = ((ty.ok >> ky) & (tx.ok >> kx) & 1u) != 0;
+                wt[j][t] = ty.w[ky] * tx.w[kx];
+                okm[j] |= (ok ? 1u : 0u) << t;
+                if (S) {
+                    // slab rows are clamped into the loaded range, so a read
+                    // can never leave the stage
+                    const int row = min(max(ty.idx[ky] - r0, 0), rows - 1);
+                    off[j][t] = ok ? (uint32_t)(row * Wi + tx.idx[kx]) * (uint32_t)sizeof(T)
+                                   : data_bytes;   // the zero pad
+                } else {
+                    off[j][t] = (uint32_t)(ty.idx[ky] * Wi + tx.idx[kx]) * (uint32_t)sizeof(T);
+                }
+            }
+        }
+    }
+
+    T *__restrict__ Yn = Y + (int64_t)n * a.C * a.out_plane + (int64_t)h0 * Wo;
+    if (S == 0) {
+        const unsigned char *Xb =
+            reinterpret_cast<const unsigned char *>(X + (int64_t)n * a.C * a.in_plane);
+        const int64_t in_bytes = a.in_plane * (int64_t)sizeof(T);
+        for (int c = 0; c < a.C; ++c) {
+#pragma unroll
+            for (int j = 0; j < kBandPPT; ++j) {
+                if (pos[j] < 0) continue;
+                float acc = 0.0f;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float v = ((okm[j] >> t) & 1u)
+                        ? IO<T>::ld(reinterpret_cast<const T *>(Xb + off[j][t])) : 0.0f;
+                    acc = fmaf(wt[j][t], v, acc);
+                }
+                Yn[pos[j]] = IO<T>::st(acc);
+            }
+            Xb += in_bytes;
+            Yn += a.out_plane;
+        }
+        return;
+    }
+
+    // zero pads (generic writes; the copies never touch them)
+    for (int e = tid; e < S * (kBandZeroPad / 4); e += kBandThreads) {
+        const int st = e / (kBandZeroPad / 4), k = e - st * (kBandZeroPad / 4);
+        *reinterpret_cast<uint32_t *>(band_smem + (size_t)st * stage_bytes + data_bytes + 4 * k) = 0u;
+    }
+    __syncthreads();
+
+    const T *Xr = X + (int64_t)n * a.C * a.in_plane + (int64_t)r0 * Wi;
+    if (tid == 0) {
+        for (int s = 0; s < S && s < a.C; ++s) {
+            mbar_arrive_expect_tx(&full[s], data_bytes);
+            bulk_copy_g2s(band_smem + (size_t)s * stage_bytes, Xr + (int64_t)s * a.in_plane,
+                          data_bytes, &full[s]);
+        }
+    }
+    const uint32_t ring = smem_u32(band_smem);
+    int c = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    if (npos == kBandThreads * kBandPPT && S >= 4) {
+        // Full band, deep ring: two channels per pair of barriers, and no
+        // per-position bounds checks.
+        for (; c + 1 < a.C; c += 2) {
+            int s2 = s + 1;
+            uint32_t p2 = parity;
+            if (s2 == S) {
+                s2 = 0;
+                p2 ^= 1u;
+            }
+            if (!mbar_wait_bounded(&full[s], parity, a.err)) s_abort = 1;
+            if (!mbar_wait_bounded(&full[s2], p2, a.err)) s_abort = 1;
+            __syncthreads();   // every thread has waited (or given up) on both stages
+            if (s_abort) break;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t base = ring + (uint32_t)(k ? s2 : s) * stage_bytes;
+#pragma unroll
+                for (int j = 0; j < kBandPPT; ++j) {
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
+                    Yn[pos[j]] = IO<T>::st(acc);
+                }
+                Yn += a.out_plane;
+            }
+            __syncthreads();   // both stages fully read
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                if (c + S < a.C) {
+                    mbar_arrive_expect_tx(&full[s], data_bytes);
+                    bulk_copy_g2s(band_smem + (size_t)s * stage_bytes,
+                                  Xr + (int64_t)(c + S) * a.in_plane, data_bytes, &full[s]);
+                }
+                if (c + 1 + S < a.C) {
+                    mbar_arrive_expect_tx(&full[s2], data_bytes);
+                    bulk_copy_g2s(band_smem + (size_t)s2 * stage_bytes,
+                                  Xr + (int64_t)(c + 1 + S) * a.in_plane, data_bytes, &full[s2]);
+                }
+            }
+            s = s2 + 1;
+            parity = p2;
+            if (s == S) {
+                s = 0;
+                parity ^= 1u;
+            }
+        }
+    }
+    for (; c < a.C && !s_abort; ++c) {
+        if (!mbar_wait_bounded(&full[s], parity, a.err)) s_abort = 1;
+        __syncthreads();   // every thread has waited (or given up) on stage s
+        if (s_abort) break;
+        const uint32_t base = ring + (uint32_t)s * stage_bytes;
+#pragma unroll
+        for (int j = 0; j < kBandPPT; ++j) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
+            if (pos[j] >= 0) Yn[pos[j]] = IO<T>::st(acc);
+        }
+        Yn += a.out_plane;
+        __syncthreads();   // stage s fully read
+        if (tid == 0 && c + S < a.C) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&full[s], data_bytes);
+            bulk_copy_g2s(band_smem + (size_t)s * stage_bytes, Xr + (int64_t)(c + S) * a.in_plane,
+                          data_bytes, &full[s]);
+        }
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+    if (c < a.C && tid == 0) {
+        // a wait gave up: let the copies still in flight land before the
+        // block's shared memory is released (bounded again)
+        for (int cc = c; cc < a.C && cc < c + S; ++cc)
+            mbar_wait_bounded(&full[cc % S], (uint32_t)(cc / S) & 1u, nullptr);
+    }
+}
+
+// Host side: use the band kernel when rows can be bulk-copied (16-byte
+// multiples and alignment) and a band of whole output rows fits 1024
+// positions; *used tells the caller whether it ran.
+template <typename T, int MODE>
+cudaError_t launch_band(const void *X, const void *theta, void *Y, const SampleParams &P,
+                        cudaStream_t s, bool *used) {
+    *used = false;
+    const SampleArgs &a = P.a;
+    const int Wi = a.in[1], Wo = a.out[1];
+    const size_t row_bytes = (size_t)Wi * sizeof(T);
+    if (row_bytes % 16 != 0 || (uintptr_t)X % 16 != 0) return cudaSuccess;
+    if (Wo > kBandThreads * kBandPPT) return cudaSuccess;
+    constexpr int kRingBytes = 48 * 1024;   // four blocks per SM (with the register bound)
+    if ((size_t)kRingBytes < (size_t)kBandMinStages * (4 * row_bytes + kBandZeroPad))
+        return cudaSuccess;                 // rows too wide to stage usefully
+    BandParams B;
+    B.th = min(a.out[0], (kBandThreads * kBandPPT) / Wo);
+    B.bands = (a.out[0] + B.th - 1) / B.th;
+    B.ring_bytes = kRingBytes;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            band_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const unsigned blocks = (unsigned)((int64_t)a.N * B.bands);
+    band_kernel<T, MODE><<<blocks, kBandThreads, kRingBytes, s>>>((const T *)X, (const T *)theta,
+                                                                   (T *)Y, P, B);
+    *used = true;
+    return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -38,6 +38,7 @@ template <> struct IO<__half> {
     static __device__ __forceinline__ float ld(const __half *p) { return __half2float(__ldg(p)); }
     static __device__ __forceinline__ __half st(float v) { return __float2half_rn(v); }
     static __device__ __forceinline__ double to_double(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
 };
 template <> struct IO<__nv_bfloat16> {
     static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) {
@@ -47,6 +48,7 @@ template <> struct IO<__nv_bfloat16> {
     static __device__ __forceinline__ double to_double(__nv_bfloat16 v) {
         return __bfloat162float(v);
     }
+    static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
 // ------------------------------------------------------------- axis params

@@ -21,6 +21,7 @@ struct SampleArgs {
     int tiles;           // blocks per image: ceil(out_plane / kSampleThreads)
     int pad, ac;
     float a;             // Keys coefficient
+    unsigned *err;       // device error word (bounded waits record timeouts here)
 };
 
 // Arguments of the standalone AffineGrid kernel.

@@ -100,21 +100,31 @@ def test_affine_sample_sweep(gs_cuda, oracle_mod, r, mode, pad, ac, dtype):
     Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), mode, pad, ac)
     ref = oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, pad, ac)
     if mode == "nearest":
-        # Away from half-integer positions the chosen index is unique and the
-        # output is a bit copy; within 1e-7 px of a tie either neighbour is a
-        # rounding of the same exact position, so only membership is checked.
-        grid = oracle_mod.affine_grid(exact(Tt), size, ac)
-        tie = np.zeros(grid.shape[:-1], dtype=bool)
-        for d in range(r):
-            n = xs[2 + d]
-            gd = grid[..., r - 1 - d]
-            x = (gd + 1) / 2 * (n - 1) if ac else ((gd + 1) * n - 1) / 2
-            tie |= np.abs(x - np.floor(x) - 0.5) < 1e-7
-        tie = np.broadcast_to(tie[:, None], ref.shape)
-        got = exact(Y)
-        np.testing.assert_array_equal(got[~tie], ref[~tie])
+        assert_nearest_affine(oracle_mod, Y, ref, Tt, size, xs, ac)
     else:
         assert_parity(Y, ref, dtype, f"affine r={r} {mode} {pad} ac={ac} {dtype}")
+
+
+def assert_nearest_affine(oracle_mod, Y, ref, Tt, size, xs, ac):
+    """Nearest on an affine map: bit copies away from half-integer positions.
+
+    Where the exact position is k + 1/2 but the map's coefficients are not
+    dyadic (e.g. a 1/37 scale), neither the fp64 oracle nor the fixed-point
+    kernel forms the tie exactly, and each rounds it by its own rounding
+    error; within 1e-7 px of a tie only membership in X (or 0) is checked.
+    """
+    r = len(xs) - 2
+    grid = oracle_mod.affine_grid(exact(Tt), size, ac)
+    tie = np.zeros(grid.shape[:-1], dtype=bool)
+    for d in range(r):
+        n = xs[2 + d]
+        gd = grid[..., r - 1 - d]
+        x = (gd + 1) / 2 * (n - 1) if ac else ((gd + 1) * n - 1) / 2
+        tie |= np.abs(x - np.floor(x) - 0.5) < 1e-7
+    tie = np.broadcast_to(tie[:, None], ref.shape)
+    got = exact(Y)
+    np.testing.assert_array_equal(got[~tie], ref[~tie])
+    return tie
 
 
 @pytest.mark.parametrize("r,ac,dtype", list(itertools.product((2, 3), (0, 1), DTYPES)))
@@ -309,3 +319,63 @@ def test_full_size_gs2d_small(gs_cuda, oracle_mod):
     Y = gs_cuda.gs_grid_sample(Xt.cuda(), Gt.cuda(), w.mode, w.padding_mode, w.align_corners)
     assert_parity(Y, oracle_mod.grid_sample(exact(Xt), exact(Gt), w.mode, w.padding_mode,
                                             w.align_corners), "float32", "gs2d_small")
+
+
+# ------------------------------------------------ fused 2-D footprint cases
+
+def _footprint_thetas(n):
+    """identity-ish, pushed off the bottom, pushed off the top and rotated, zoomed out."""
+    base = [[[1.02, 0.03, 0.01], [-0.02, 0.98, 0.02]],
+            [[1.0, 0.05, 0.1], [0.06, 1.0, 0.6]],
+            [[0.95, -0.2, -0.05], [0.25, 1.05, -0.7]],
+            [[2.5, 0.0, 0.0], [0.0, 2.5, 0.0]]]
+    return np.array([base[i % 4] for i in range(n)])
+
+
+@pytest.mark.parametrize("mode", ["linear", "nearest", "cubic"])
+@pytest.mark.parametrize("pad", ["zeros", "border", "reflection"])
+@pytest.mark.parametrize("ac", [0, 1])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_affine_footprint_cases(gs_cuda, oracle_mod, mode, pad, ac, dtype):
+    """Bands pushed off either edge, rotated, zoomed out; a ragged tile tail."""
+    g = wl.rng(zlib.crc32(repr((mode, pad, ac, dtype, "footprint")).encode()))
+    xs = (4, 5, 40, 32)            # 5 channels: not a multiple of the ring depth
+    size = (4, 5, 37, 48)          # 1776 positions: a ragged last tile
+    Tt = wl.as_dtype(_footprint_thetas(4), dtype)
+    Xt = wl.as_dtype(g.normal(size=xs), dtype)
+    Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), mode, pad, ac)
+    ref = oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, pad, ac)
+    if mode == "nearest":
+        tie = assert_nearest_affine(oracle_mod, Y, ref, Tt, size, xs, ac)
+        assert tie.any()   # the zoomed image puts a whole row on exact ties
+    else:
+        assert_parity(Y, ref, dtype, f"footprint {mode} {pad} ac={ac} {dtype}")
+
+
+@pytest.mark.parametrize("mode", ["linear", "cubic"])
+def test_affine_tall_input_zoomed_and_transposed(gs_cuda, oracle_mod, mode):
+    g = wl.rng(17)
+    xs = (2, 3, 420, 32)
+    size = (2, 3, 30, 40)
+    theta = np.array([[[1.5, 0.0, 0.0], [0.0, 1.5, 0.0]], [[0.3, 1.2, 0.1], [1.3, 0.2, -0.1]]])
+    Tt, Xt = wl.as_dtype(theta, "float32"), wl.as_dtype(g.normal(size=xs), "float32")
+    for pad in ("zeros", "border", "reflection"):
+        Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), mode, pad, 0)
+        assert_parity(Y, oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, pad, 0),
+                      "float32", f"tall {mode} {pad}")
+        assert gs_cuda.gs_device_status() == 0
+
+
+def test_results_do_not_depend_on_input_alignment(gs_cuda):
+    """An X view offset by one element gives bit-identical results."""
+    w = wl.WORKLOADS["stn2d"]
+    inp = wl.make_affine_sample_inputs(w, x_shape=(8, 6, 128, 128))
+    for dtype in ("float32", "bfloat16"):
+        Tt, Xt = dev(inp["theta"], dtype), dev(inp["X"], dtype)
+        base = torch.empty(Xt.numel() + 8, dtype=Xt.dtype, device="cuda")
+        Xm = base[1:1 + Xt.numel()].view_as(Xt)
+        Xm.copy_(Xt)
+        size = (8, 6, 128, 128)
+        Yb = gs_cuda.gs_affine_sample(Tt, size, Xt, "linear", "border", 1)
+        Yg = gs_cuda.gs_affine_sample(Tt, size, Xm, "linear", "border", 1)
+        assert torch.equal(Yb, Yg), dtype
