@@ -210,6 +210,7 @@ gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, i
     a.dH = (int)at->dilations[0]; a.dW = (int)at->dilations[1];
     a.group = (int)at->group; a.offset_group = (int)at->offset_group;
     a.has_bias = B != nullptr; a.has_mask = mask != nullptr;
+    a.err = error_word();
     return dispatch(dt, [&](auto tag) {
         return gs::launch_deform<decltype(tag)>(X, W, offset, B, mask, Y, a, stream);
     });

@@ -1,4 +1,5 @@
-// gs_deform.cuh -- DeformConv 2-D with fp32 FMAs (all dtypes, all attributes).
+// gs_deform.cuh -- DeformConv 2-D with fp32 FMAs (every dtype and attribute;
+// fp16/bf16 shapes the tensor-core kernel in gs_deform_tc.cuh covers go there).
 //
 // DeformConv (ai.onnx, since version 22), Inputs: the output is an ordinary
 // convolution over a column of samples, each a bilinear read of X at the
@@ -14,7 +15,10 @@
 // one position and kOCB/4 output channels).
 #pragma once
 
+#include <type_traits>
+
 #include "gs_common.cuh"
+#include "gs_deform_tc.cuh"
 #include "gs_internal.h"
 
 namespace gs {
@@ -177,6 +181,12 @@ deform_simt_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *_
 template <typename T>
 cudaError_t launch_deform(const void *X, const void *W, const void *offset, const void *B,
                           const void *mask, void *Y, const DeformArgs &a, cudaStream_t s) {
+    if constexpr (!std::is_same<T, float>::value) {
+        // half types: contraction on the tensor cores where the shape allows
+        bool used = false;
+        const cudaError_t e = launch_deform_tc<T>(X, W, offset, B, mask, Y, a, s, &used);
+        if (used || e != cudaSuccess) return e;
+    }
     const int P = a.oH * a.oW;
     const int pos_tiles = (P + kDTP - 1) / kDTP;
     const int oCg = a.oC / a.group;

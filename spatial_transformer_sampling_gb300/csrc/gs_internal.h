@@ -37,6 +37,7 @@ struct DeformArgs {
     int N, C, H, W, oC, oH, oW;
     int kH, kW, pad_t, pad_l, sH, sW, dH, dW, group, offset_group;
     int has_bias, has_mask;
+    unsigned *err;       // device error word (bounded waits record timeouts here)
 };
 
 // Per-dtype launchers; T is float, __half or __nv_bfloat16.  Each enqueues on

@@ -87,3 +87,97 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
 }
 
 }  // namespace gs
+
+// ------------------------------------------------------------------ tcgen05
+//
+// Fifth-generation tensor-core MMA with the accumulator in tensor memory
+// (TMEM).  Operands are read from shared memory through 64-bit matrix
+// descriptors; one thread issues the MMAs, completion is signalled on an
+// mbarrier by tcgen05.commit, and the accumulator is read back with
+// tcgen05.ld.
+
+namespace gs {
+
+// Shared-memory matrix descriptor, K-major operand without swizzling: the
+// tile is made of 8-row x 16-byte core matrices (each 128 contiguous bytes);
+// `lbo` is the byte distance between core matrices adjacent along K, `sbo`
+// between core matrices adjacent along M (or N).
+__device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t smem_addr, uint32_t lbo,
+                                                     uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;          // leading-dimension byte offset
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;          // stride-dimension byte offset
+    d |= (uint64_t)1 << 46;                               // descriptor version for tcgen05
+    // base offset 0, relative leading-dimension offsets, no swizzling (bits 61-63 = 0)
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, A and B both bf16
+// (is_bf16) or both fp16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(bool is_bf16, int M, int N) {
+    return (1u << 4)                                    // D format: fp32
+           | ((is_bf16 ? 1u : 0u) << 7)                 // A format
+           | ((is_bf16 ? 1u : 0u) << 10)                // B format
+           | ((uint32_t)(N >> 3) << 17)                 // N / 8
+           | ((uint32_t)(M >> 4) << 24);                // M / 16
+}
+
+// Allocate `ncols` TMEM columns (a power of two >= 32); the whole warp calls
+// it; the TMEM address lands in shared memory at `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for one M x N x 16 step.
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tcgen05_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tcgen05_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// Eight consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace gs

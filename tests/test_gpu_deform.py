@@ -88,3 +88,38 @@ def test_full_size_deform2d(gs_cuda, oracle_mod, dtype):
     ref = oracle_mod.deform_conv_at(exact(host["X"]), exact(host["W"]), exact(host["offset"]), idx,
                                     exact(host["B"]), exact(host["mask"]), **kw)
     assert_parity(Y.reshape(-1)[torch.from_numpy(idx).cuda()], ref, dtype, "deform2d sampled")
+
+
+# shapes the tensor-core kernel takes (group = offset_group = 1, C and oC multiples of 16)
+TC_CASES = [
+    # N, C, H, W, oC, kernel, pads, strides, dilations, bias, mask
+    (2, 32, 13, 11, 16, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True),     # ragged last tile
+    (1, 48, 9, 17, 32, (3, 2), (0, 1, 2, 0), (2, 1), (1, 2), False, True),    # 16-channel chunks
+    (1, 128, 12, 12, 48, (1, 1), (0, 0, 0, 0), (1, 1), (1, 1), True, False),  # 64-channel chunks
+    (1, 64, 16, 16, 128, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True),   # N = 128
+    (3, 96, 7, 9, 64, (2, 2), (1, 0, 0, 1), (1, 1), (2, 1), True, True),      # 32-channel chunks
+]
+
+
+@pytest.mark.parametrize("case,dtype", list(itertools.product(range(len(TC_CASES)),
+                                                              ["float16", "bfloat16"])))
+def test_deform_conv_tensor_core_shapes(gs_cuda, oracle_mod, case, dtype):
+    N, C, H, W, oC, k, p, s, d, has_b, has_m = TC_CASES[case]
+    g = wl.rng(500 + case)
+    oH = (H + p[0] + p[2] - d[0] * (k[0] - 1) - 1) // s[0] + 1
+    oW = (W + p[1] + p[3] - d[1] * (k[1] - 1) - 1) // s[1] + 1
+    K = k[0] * k[1]
+    host = {
+        "X": wl.as_dtype(g.normal(size=(N, C, H, W)), dtype),
+        "W": wl.as_dtype(g.normal(0, 0.05, size=(oC, C) + k), dtype),
+        "offset": wl.as_dtype(g.normal(0, 1.0, size=(N, K * 2, oH, oW)), dtype),
+        "B": wl.as_dtype(g.normal(size=(oC,)), dtype) if has_b else None,
+        "mask": wl.as_dtype(g.uniform(0, 1, size=(N, K, oH, oW)), dtype) if has_m else None,
+    }
+    kw = dict(kernel_shape=k, pads=p, strides=s, dilations=d)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Y, ref, dtype, f"deform tc case {case} {dtype}")
