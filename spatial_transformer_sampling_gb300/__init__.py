@@ -13,13 +13,18 @@ Operators (see the docstrings and include/gs.h):
                    zeros / border / reflection; both align_corners)
   gs_affine_sample GridSample(X, AffineGrid(theta, size)) fused
   gs_deform_conv   DeformConv 2-D
+
+Host-memory variants (gs_affine_sample_from_host, gs_grid_sample_from_host)
+stream a batch from pinned host memory in chunks, overlapping the copies in
+both directions with the kernels.
 """
 import ctypes
 import os
 
 __all__ = ["gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
            "gs_status_str", "gs_device_status", "GsError", "library_path", "load_library",
-           "EXPORTED_SYMBOLS"]
+           "EXPORTED_SYMBOLS", "HostStreamer", "gs_affine_sample_from_host",
+           "gs_grid_sample_from_host"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libgs.so")
@@ -213,3 +218,100 @@ def gs_device_status(device=None):
     torch = _torch()
     s = torch.cuda.current_stream(device).cuda_stream
     return load_library().gs_device_status(ctypes.c_void_p(s))
+
+
+class HostStreamer:
+    """Run a batch whose inputs and output live in pinned host memory, chunked over
+    the batch axis so the host-to-device copies of chunk i+1, the kernel on chunk
+    i and the device-to-host copy of chunk i-1 overlap on three CUDA streams.
+
+    The operators are independent per image, so chunking over N changes nothing
+    in the result.  Device buffers are allocated once per shape and reused.
+    """
+
+    def __init__(self, device=None, chunks=8):
+        torch = _torch()
+        self.device = torch.device(device or "cuda")
+        self.chunks = int(chunks)
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_run = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
+        self._dev = {}
+
+    def _buffers(self, key, shapes, dtype):
+        torch = _torch()
+        if key not in self._dev:
+            self._dev[key] = [torch.empty(s, dtype=dtype, device=self.device) for s in shapes]
+        return self._dev[key]
+
+    def run(self, fn, inputs, out_host, batch_axes):
+        """fn(*device_chunks, out=device_out_chunk) on chunks along each input's batch axis
+        (batch_axes[i] is None for inputs passed whole); out_host is filled in place."""
+        torch = _torch()
+        N = out_host.shape[0]
+        step = max(1, -(-N // self.chunks))
+        key = (tuple((tuple(t.shape), t.dtype) for t in inputs), tuple(out_host.shape),
+               out_host.dtype)
+        dev = self._buffers(key, [t.shape for t in inputs] + [out_host.shape], out_host.dtype)
+        d_in, d_out = dev[:-1], dev[-1]
+        cur = torch.cuda.current_stream(self.device)
+        for s in (self.s_in, self.s_run, self.s_out):
+            s.wait_stream(cur)
+        for n0 in range(0, N, step):
+            n1 = min(N, n0 + step)
+            with torch.cuda.stream(self.s_in):
+                parts = []
+                for t, d, ax in zip(inputs, d_in, batch_axes):
+                    if ax is None:
+                        if n0 == 0:
+                            d.copy_(t, non_blocking=True)
+                        parts.append(d)
+                    else:
+                        d[n0:n1].copy_(t[n0:n1], non_blocking=True)
+                        parts.append(d[n0:n1])
+                ev_in = torch.cuda.Event()
+                ev_in.record(self.s_in)
+            with torch.cuda.stream(self.s_run):
+                self.s_run.wait_event(ev_in)
+                fn(*parts, out=d_out[n0:n1])
+                ev_run = torch.cuda.Event()
+                ev_run.record(self.s_run)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(ev_run)
+                out_host[n0:n1].copy_(d_out[n0:n1], non_blocking=True)
+        for s in (self.s_in, self.s_run, self.s_out):
+            cur.wait_stream(s)
+        return out_host
+
+
+def gs_affine_sample_from_host(theta, size, X, mode="linear", padding_mode="zeros",
+                               align_corners=0, cubic_coeff_a=-0.75, out=None, streamer=None):
+    """gs_affine_sample with theta, X and the output in (pinned) host memory,
+    copies overlapped with the kernels; returns the host output, complete once the
+    current CUDA stream reaches this point (synchronize before reading it)."""
+    torch = _torch()
+    size = [int(s) for s in size]
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + size[2:], dtype=X.dtype).pin_memory()
+    st = streamer or HostStreamer(chunks=8)
+
+    def fn(th, x, out):
+        n = x.shape[0]
+        return gs_affine_sample(th, [n] + size[1:], x, mode, padding_mode, align_corners,
+                                cubic_coeff_a, out=out)
+    return st.run(fn, [theta, X], out, [0, 0])
+
+
+def gs_grid_sample_from_host(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
+                             cubic_coeff_a=-0.75, out=None, streamer=None):
+    """gs_grid_sample with X, grid and the output in (pinned) host memory, copies
+    overlapped with the kernels; returns the host output, complete once the current
+    CUDA stream reaches this point (synchronize before reading it)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + list(grid.shape[1:-1]), dtype=X.dtype).pin_memory()
+    st = streamer or HostStreamer(chunks=8)
+
+    def fn(x, g, out):
+        return gs_grid_sample(x, g, mode, padding_mode, align_corners, cubic_coeff_a, out=out)
+    return st.run(fn, [X, grid], out, [0, 0])
