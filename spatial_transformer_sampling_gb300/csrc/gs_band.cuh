@@ -98,6 +98,12 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
                 ymin = y < ymin ? y : ymin;
                 ymax = y > ymax ? y : ymax;
             }
+            if (MODE != MODE_CUBIC && a.pad == PAD_BORDER) {
+                // linear/nearest clamp the coordinate before taking taps: a
+                // clamped position keeps its (zero-weight) second tap
+                ymin = clamp_q(ymin, 0, P.ax[0].hi_q);
+                ymax = clamp_q(ymax, 0, P.ax[0].hi_q);
+            }
             lo = (int)(ymin >> 32) - (MODE == MODE_CUBIC ? 1 : 0);
             hi = (int)(ymax >> 32) + (MODE == MODE_CUBIC ? 2 : 1);
             if (a.pad == PAD_REFLECTION && (lo < 0 || hi > Hi - 1)) {

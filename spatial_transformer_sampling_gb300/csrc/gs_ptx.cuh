@@ -10,7 +10,7 @@
 namespace gs {
 
 // Device error word bits (see gs_device_status in include/gs.h).
-constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrTimeout = 1u;    // a bounded wait gave up
 
 // A wait gives up after this long (ns of %globaltimer); copies land in
 // microseconds, so only a broken pipeline ever reaches it.

@@ -379,3 +379,46 @@ def test_results_do_not_depend_on_input_alignment(gs_cuda):
         Yb = gs_cuda.gs_affine_sample(Tt, size, Xt, "linear", "border", 1)
         Yg = gs_cuda.gs_affine_sample(Tt, size, Xm, "linear", "border", 1)
         assert torch.equal(Yb, Yg), dtype
+
+
+# ------------------------------------------------ fused 3-D footprint cases
+
+def _footprint_thetas_3d(n):
+    base = [[[1.02, 0.03, -0.05, 0.01], [-0.04, 0.98, 0.06, 0.02], [0.05, -0.03, 1.01, -0.03]],
+            [[1.0, 0.05, 0.0, 0.1], [0.06, 1.0, 0.0, 0.6], [0.0, 0.1, 1.0, -0.7]],
+            [[0.95, -0.2, 0.1, -0.05], [0.25, 1.05, -0.1, -0.3], [-0.1, 0.15, 0.9, 0.2]],
+            [[2.5, 0.0, 0.0, 0.0], [0.0, 2.5, 0.0, 0.0], [0.0, 0.0, 2.5, 0.0]]]
+    return np.array([base[i % 4] for i in range(n)])
+
+
+@pytest.mark.parametrize("mode", ["linear", "nearest"])
+@pytest.mark.parametrize("pad", ["zeros", "border", "reflection"])
+@pytest.mark.parametrize("ac", [0, 1])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_affine3d_footprint_cases(gs_cuda, oracle_mod, mode, pad, ac, dtype):
+    """Rows of 16-byte multiples: several tiles, ragged in depth and rows."""
+    g = wl.rng(zlib.crc32(repr((mode, pad, ac, dtype, "footprint3")).encode()))
+    xs = (4, 3, 12, 10, 16)
+    size = (4, 3, 20, 30, 24)
+    Tt = wl.as_dtype(_footprint_thetas_3d(4), dtype)
+    Xt = wl.as_dtype(g.normal(size=xs), dtype)
+    Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), mode, pad, ac)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, pad, ac)
+    if mode == "nearest":
+        assert_nearest_affine(oracle_mod, Y, ref, Tt, size, xs, ac)
+    else:
+        assert_parity(Y, ref, dtype, f"3d footprint {mode} {pad} ac={ac} {dtype}")
+
+
+@pytest.mark.parametrize("pad", ["zeros", "border", "reflection"])
+def test_affine3d_box_too_large_gathers_instead(gs_cuda, oracle_mod, pad):
+    g = wl.rng(23)
+    xs = (1, 2, 40, 40, 32)            # a zoomed-out tile needs the whole 205 KB volume
+    size = (1, 2, 10, 12, 16)
+    theta = np.array([[[1.6, 0.0, 0.0, 0.0], [0.0, 1.6, 0.0, 0.0], [0.0, 0.0, 1.6, 0.0]]])
+    Tt, Xt = wl.as_dtype(theta, "float32"), wl.as_dtype(g.normal(size=xs), "float32")
+    Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), "linear", pad, 1)
+    assert gs_cuda.gs_device_status() == 0
+    assert_parity(Y, oracle_mod.affine_sample(exact(Tt), size, exact(Xt), "linear", pad, 1),
+                  "float32", f"3d gather fallback {pad}")
