@@ -12,8 +12,9 @@
  *    even on store.
  *  - The library allocates no memory, keeps no state between calls and never
  *    synchronises: every call only enqueues kernels on `stream` (0 = the
- *    legacy default stream) and returns.  Output buffers must not overlap
- *    inputs.
+ *    legacy default stream) and returns.  Scratch space, where a path uses
+ *    some, is a workspace the caller passes in.  Output buffers must not
+ *    overlap inputs.
  *  - Arguments are checked on the host before anything is enqueued; a bad
  *    argument returns its gs_status and leaves the outputs untouched.  A
  *    failed launch returns GS_ERR_CUDA.  A tensor with a zero extent is valid
@@ -100,6 +101,40 @@ gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *s
 gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const void *grid,
                          const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
                          int align_corners, float cubic_coeff_a, void *Y, cudaStream_t stream);
+
+/*
+ * gs_grid_sample_workspace_size -- device workspace that gs_grid_sample_ws
+ * asks for with these shapes: a whole number of channel-last images (at least
+ * one, about 32 MB at most).  0 means the call never uses a workspace (rank
+ * other than 2, C * element size not a multiple of 16 bytes, C*H*W >= 2^31, or
+ * an empty tensor).  Arguments as gs_grid_sample; `bytes` is a host output.
+ * Shape errors are reported as by gs_grid_sample.
+ */
+gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int64_t *out_spatial,
+                                        gs_dtype dt, size_t *bytes);
+
+/*
+ * gs_grid_sample_ws -- gs_grid_sample with a caller-owned device workspace
+ * (GridSample - version 20, as above; the same results, value for value).
+ *
+ *   workspace        device, 16-byte aligned (GS_ERR_ALIGN), or NULL.
+ *   workspace_bytes  its size.  With at least one image's worth (C*H*W
+ *                    elements of `dt`), 2-D calls copy X to channel-last order
+ *                    there, as many whole images at a time as it holds, and
+ *                    read every tap as 16-byte runs of channels: for grids
+ *                    without spatial locality this cuts the bytes read per
+ *                    output several fold.  The size that
+ *                    gs_grid_sample_workspace_size gives keeps a chunk
+ *                    resident in L2; a larger one is allowed but not faster.
+ *                    With less than one image, or NULL, it is gs_grid_sample.
+ *
+ * The workspace's contents on entry do not matter and are garbage on return.
+ * Calls on different streams must not share a workspace while in flight.
+ */
+gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const void *grid,
+                            const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                            int align_corners, float cubic_coeff_a, void *workspace,
+                            size_t workspace_bytes, void *Y, cudaStream_t stream);
 
 /*
  * gs_affine_sample -- GridSample(X, AffineGrid(theta, size)) in one kernel:

@@ -70,6 +70,9 @@ def load_library(path=None):
     ci, cf = ctypes.c_int, ctypes.c_float
     L.gs_affine_grid.argtypes = [vp, ci, ci, i64p, ci, vp, vp]
     L.gs_grid_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
+    L.gs_grid_sample_workspace_size.argtypes = [i64p, ci, i64p, ci, ctypes.POINTER(ctypes.c_size_t)]
+    L.gs_grid_sample_ws.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, ctypes.c_size_t,
+                                    vp, vp]
     L.gs_affine_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
     L.gs_deform_conv.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
                                  ctypes.POINTER(DeformAttrs), ci, vp, vp]
@@ -77,8 +80,8 @@ def load_library(path=None):
     L.gs_status_str.restype = ctypes.c_char_p
     L.gs_device_status.argtypes = [vp]
     L.gs_version.restype = ctypes.c_char_p
-    for f in ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
-              "gs_device_status"):
+    for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
+              "gs_grid_sample_ws", "gs_affine_sample", "gs_deform_conv", "gs_device_status"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -149,18 +152,63 @@ def gs_affine_grid(theta, size, align_corners=0, out=None):
 
 
 def gs_grid_sample(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
-                   cubic_coeff_a=-0.75, out=None):
-    """GridSample: X (N, C, in...), grid (N, out..., r) -> Y (N, C, out...)."""
+                   cubic_coeff_a=-0.75, out=None, workspace=None):
+    """GridSample: X (N, C, in...), grid (N, out..., r) -> Y (N, C, out...).
+
+    ``workspace``: None calls gs_grid_sample; a device tensor (any dtype, used as
+    raw bytes) or "auto" (one of the size gs_grid_sample_workspace_size asks
+    for, from torch's allocator) calls gs_grid_sample_ws."""
     torch = _torch()
     _check_tensors(X, grid, out)
     r = X.dim() - 2
     out_sp = list(grid.shape[1:-1])
     if out is None:
         out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
+    if workspace is not None:
+        return gs_grid_sample_ws(X, grid, workspace, mode, padding_mode, align_corners,
+                                 cubic_coeff_a, out)
     _ok(load_library().gs_grid_sample(_ptr(X), _i64(X.shape), r, _ptr(grid), _i64(out_sp),
                                       _dtype_code(X), MODES[mode], PADS[padding_mode],
                                       int(align_corners), float(cubic_coeff_a), _ptr(out),
                                       _stream(X)), "gs_grid_sample")
+    return out
+
+
+def gs_grid_sample_workspace_size(x_shape, out_spatial, dtype):
+    """Workspace bytes gs_grid_sample_ws asks for (0: the shape never uses one)."""
+    torch = _torch()
+    code = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[dtype]
+    n = ctypes.c_size_t(0)
+    _ok(load_library().gs_grid_sample_workspace_size(_i64(x_shape), len(x_shape) - 2,
+                                                     _i64(out_spatial), code, ctypes.byref(n)),
+        "gs_grid_sample_workspace_size")
+    return int(n.value)
+
+
+def gs_grid_sample_ws(X, grid, workspace="auto", mode="linear", padding_mode="zeros",
+                      align_corners=0, cubic_coeff_a=-0.75, out=None):
+    """gs_grid_sample with a device workspace (see gs_grid_sample_ws in gs.h)."""
+    torch = _torch()
+    _check_tensors(X, grid, out)
+    r = X.dim() - 2
+    out_sp = list(grid.shape[1:-1])
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError(f"workspace must be a tensor, None or 'auto', not {workspace!r}")
+        nbytes = gs_grid_sample_workspace_size(X.shape, out_sp, X.dtype)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=X.device) if nbytes else None
+    if workspace is not None:
+        if not workspace.is_cuda or workspace.device != X.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on X's device")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    else:
+        ws_ptr, ws_bytes = None, 0
+    _ok(load_library().gs_grid_sample_ws(_ptr(X), _i64(X.shape), r, _ptr(grid), _i64(out_sp),
+                                         _dtype_code(X), MODES[mode], PADS[padding_mode],
+                                         int(align_corners), float(cubic_coeff_a), ws_ptr,
+                                         ws_bytes, _ptr(out), _stream(X)), "gs_grid_sample_ws")
     return out
 
 
@@ -303,15 +351,24 @@ def gs_affine_sample_from_host(theta, size, X, mode="linear", padding_mode="zero
 
 
 def gs_grid_sample_from_host(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
-                             cubic_coeff_a=-0.75, out=None, streamer=None):
+                             cubic_coeff_a=-0.75, out=None, streamer=None, workspace=None):
     """gs_grid_sample with X, grid and the output in (pinned) host memory, copies
     overlapped with the kernels; returns the host output, complete once the current
-    CUDA stream reaches this point (synchronize before reading it)."""
+    CUDA stream reaches this point (synchronize before reading it).  ``workspace``
+    as in gs_grid_sample ("auto" keeps one per streamer and chunk shape)."""
     torch = _torch()
     if out is None:
         out = torch.empty(list(X.shape[:2]) + list(grid.shape[1:-1]), dtype=X.dtype).pin_memory()
     st = streamer or HostStreamer(chunks=8)
 
     def fn(x, g, out):
-        return gs_grid_sample(x, g, mode, padding_mode, align_corners, cubic_coeff_a, out=out)
+        ws = workspace
+        if isinstance(ws, str) and ws == "auto":
+            nbytes = gs_grid_sample_workspace_size(x.shape, g.shape[1:-1], x.dtype)
+            ws = st._buffers(("workspace", nbytes), [(nbytes,)], torch.uint8)[0] if nbytes else None
+            if ws is None:
+                return gs_grid_sample(x, g, mode, padding_mode, align_corners, cubic_coeff_a,
+                                      out=out)
+        return gs_grid_sample(x, g, mode, padding_mode, align_corners, cubic_coeff_a, out=out,
+                              workspace=ws)
     return st.run(fn, [X, grid], out, [0, 0])

@@ -62,10 +62,10 @@ gs_status check_spatial(const int64_t *ext, int r, int64_t *prod, bool *empty) {
 
 bool nc_ok(int64_t N, int64_t C) { return N >= 0 && C >= 0 && N <= kMaxSlab && C <= kMaxSlab; }
 
-// Shared checks of gs_grid_sample and gs_affine_sample.
-gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64_t *out_sp,
-                       gs_dtype dt, gs_mode mode, gs_pad pad, int ac, float a, const void *Y,
-                       gs::SampleArgs *args, bool *skip) {
+// Shape and attribute checks shared by the sampling entry points (no pointers).
+gs_status check_sample_shape(const int64_t *x_shape, int r, const int64_t *out_sp, gs_dtype dt,
+                             gs_mode mode, gs_pad pad, int ac, float a, gs::SampleArgs *args,
+                             bool *skip) {
     if (!x_shape || !out_sp) return GS_ERR_NULL;
     if (!dtype_ok(dt)) return GS_ERR_DTYPE;
     if ((int)mode < GS_LINEAR || (int)mode > GS_CUBIC) return GS_ERR_ATTR;
@@ -83,8 +83,6 @@ gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64
     *skip = out_empty || N == 0 || C == 0;
     if (*skip) return GS_OK;
     if (in_empty) return GS_ERR_SHAPE;   // nothing to sample from
-    if (!X || !Y) return GS_ERR_NULL;
-    if (!aligned(X, elem_size(dt)) || !aligned(Y, elem_size(dt))) return GS_ERR_ALIGN;
     const int64_t tiles = (out_plane + gs::kSampleThreads - 1) / gs::kSampleThreads;
     if (N * tiles > kMaxSlab) return GS_ERR_SHAPE;
     args->N = (int)N;
@@ -100,6 +98,17 @@ gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64
     args->ac = ac;
     args->a = a;
     args->err = nullptr;
+    return GS_OK;
+}
+
+// All checks of gs_grid_sample and gs_affine_sample except the grid / theta.
+gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64_t *out_sp,
+                       gs_dtype dt, gs_mode mode, gs_pad pad, int ac, float a, const void *Y,
+                       gs::SampleArgs *args, bool *skip) {
+    const gs_status st = check_sample_shape(x_shape, r, out_sp, dt, mode, pad, ac, a, args, skip);
+    if (st != GS_OK || *skip) return st;
+    if (!X || !Y) return GS_ERR_NULL;
+    if (!aligned(X, elem_size(dt)) || !aligned(Y, elem_size(dt))) return GS_ERR_ALIGN;
     return GS_OK;
 }
 
@@ -146,7 +155,48 @@ gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const voi
     if (!aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
     args.err = error_word();
     return dispatch(dt, [&](auto tag) {
-        return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, stream);
+        return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, nullptr, 0,
+                                                stream);
+    });
+}
+
+gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int64_t *out_spatial,
+                                        gs_dtype dt, size_t *bytes) {
+    if (!bytes) return GS_ERR_NULL;
+    *bytes = 0;
+    if (r < 1 || r > 3) return GS_ERR_RANK;
+    gs::SampleArgs args;
+    bool skip = false;
+    // mode and padding do not change the size: check the shapes only
+    const gs_status st = check_sample_shape(x_shape, r, out_spatial, dt, GS_LINEAR, GS_PAD_ZEROS,
+                                            0, -0.75f, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    switch (dt) {
+        case GS_F32: *bytes = gs::sample_workspace_bytes<float>(args, r, false); break;
+        case GS_F16: *bytes = gs::sample_workspace_bytes<__half>(args, r, false); break;
+        default: *bytes = gs::sample_workspace_bytes<__nv_bfloat16>(args, r, false); break;
+    }
+    return GS_OK;
+}
+
+gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const void *grid,
+                            const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                            int align_corners, float cubic_coeff_a, void *workspace,
+                            size_t workspace_bytes, void *Y, cudaStream_t stream) {
+    if (r < 1 || r > 3) return GS_ERR_RANK;
+    gs::SampleArgs args;
+    bool skip = false;
+    gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,
+                                cubic_coeff_a, Y, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    if (!grid) return GS_ERR_NULL;
+    if (!aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
+    if (workspace && !aligned(workspace, 16)) return GS_ERR_ALIGN;
+    if (workspace_bytes && !workspace) return GS_ERR_NULL;
+    args.err = error_word();
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, workspace,
+                                                workspace_bytes, stream);
     });
 }
 
@@ -166,7 +216,8 @@ gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const 
     if (!aligned(theta, elem_size(dt))) return GS_ERR_ALIGN;
     args.err = error_word();
     return dispatch(dt, [&](auto tag) {
-        return gs::launch_sample<decltype(tag)>(X, theta, Y, args, r, (int)mode, true, stream);
+        return gs::launch_sample<decltype(tag)>(X, theta, Y, args, r, (int)mode, true, nullptr, 0,
+                                                stream);
     });
 }
 

@@ -42,9 +42,14 @@ struct DeformArgs {
 
 // Per-dtype launchers; T is float, __half or __nv_bfloat16.  Each enqueues on
 // `s` and returns the launch error (cudaSuccess when fine).
+// `ws`, `ws_bytes`: optional device workspace for the channel-last GridSample
+// path (NULL, or fewer bytes than one image: the NCHW gather runs instead).
 template <typename T>
 cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
-                          int mode, bool affine, cudaStream_t s);
+                          int mode, bool affine, void *ws, size_t ws_bytes, cudaStream_t s);
+// Workspace bytes the channel-last path asks for (0: this call never takes it).
+template <typename T>
+size_t sample_workspace_bytes(const SampleArgs &args, int r, bool affine);
 template <typename T>
 cudaError_t launch_affine_grid(const void *theta, void *grid, const AffineGridArgs &args, int r,
                                cudaStream_t s);

@@ -326,6 +326,7 @@ inline Axis make_axis(int n, int ac) {
 }  // namespace gs
 
 #include "gs_band.cuh"
+#include "gs_nhwc.cuh"
 
 namespace gs {
 
@@ -356,8 +357,7 @@ static cudaError_t launch_sample_mode(const void *X, const void *src, void *Y,
 }
 
 template <typename T>
-cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
-                          int mode, bool affine, cudaStream_t s) {
+static SampleParams make_params(const SampleArgs &args, int r) {
     SampleParams P;
     P.a = args;
     for (int d = 0; d < kMaxRank; ++d) {
@@ -377,10 +377,25 @@ cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleA
         P.alpha[d] = args.ac ? 0.5 * (double)(n - 1) : 0.5 * (double)n;
         P.beta[d] = 0.5 * (double)(n - 1);
     }
+    return P;
+}
+
+template <typename T>
+size_t sample_workspace_bytes(const SampleArgs &args, int r, bool affine) {
+    return nhwc_workspace_bytes<T>(args, r, affine);
+}
+
+template <typename T>
+cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
+                          int mode, bool affine, void *ws, size_t ws_bytes, cudaStream_t s) {
+    const SampleParams P = make_params<T>(args, r);
     if (affine) {
         if (r == 2) return launch_sample_mode<T, 2, true>(X, src, Y, P, mode, s);
         return launch_sample_mode<T, 3, true>(X, src, Y, P, mode, s);
     }
+    if (ws && nhwc_workspace_bytes<T>(args, r, affine) > 0 &&
+        ws_bytes >= (size_t)args.C * args.in_plane * sizeof(T))
+        return launch_nhwc<T>(X, src, Y, P, mode, ws, ws_bytes, s);
     if (r == 1) return launch_sample_mode<T, 1, false>(X, src, Y, P, mode, s);
     if (r == 2) return launch_sample_mode<T, 2, false>(X, src, Y, P, mode, s);
     return launch_sample_mode<T, 3, false>(X, src, Y, P, mode, s);
