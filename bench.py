@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--dtype", default="float32")
     p.add_argument("--mode", default=None, help="override the workload's mode")
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    p.add_argument("--workspace", action="store_true",
+                   help="GridSample workloads: gs_grid_sample_ws with the workspace it asks for")
     p.add_argument("--extra-steps", type=int, default=100)
     return p.parse_args()
 
@@ -81,6 +83,7 @@ def peaks():
 KERNEL_SOURCES = {
     "band_kernel": ["gs_band.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "sample_kernel": ["gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "nhwc_sample_kernel": ["gs_nhwc.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_internal.h"],
     "deform": ["gs_deform.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
 }
 
@@ -178,11 +181,13 @@ class ClockSampler:
 class Case:
     """One workload on one device: inputs in HBM, a launch closure, byte/flop counts."""
 
-    def __init__(self, name, dtype, device, mode=None, seed_offset=0):
+    def __init__(self, name, dtype, device, mode=None, seed_offset=0, workspace=False):
         import torch
         self.w = wl.WORKLOADS[name]
         self.name, self.dtype, self.device = name, dtype, device
         self.mode = mode or self.w.mode
+        self.ws = None
+        self.launches = 1   # kernels per step
         w = self.w
         eb = DT_BYTES[dtype]
         seed = w.seed + seed_offset
@@ -200,6 +205,15 @@ class Case:
             self.host = {"X": wl.as_dtype(inp["X"], dtype), "grid": wl.as_dtype(inp["grid"], dtype)}
             self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
             self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},grid>"
+            if workspace:
+                nbytes = gs.gs_grid_sample_workspace_size(w.x_shape, w.out_spatial,
+                                                          getattr(torch, dtype))
+                if nbytes:
+                    self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+                    slot = w.x_shape[1] * (int(np.prod(w.x_shape[2:])) + 1) * eb
+                    per = nbytes // slot
+                    self.launches = 2 * (-(-w.x_shape[0] // per))   # copy + sample per chunk
+                    self.kernel_tag = f"nhwc_sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
         else:
             inp = wl.make_deform_inputs(w, seed=seed)
             self.host = {k: wl.as_dtype(v, dtype) for k, v in inp.items()}
@@ -233,7 +247,8 @@ class Case:
                                             out=out)
         if w.kind == "grid_sample":
             return self.gs.gs_grid_sample(d["X"], d["grid"], self.mode, w.padding_mode,
-                                          w.align_corners, w.cubic_coeff_a, out=out)
+                                          w.align_corners, w.cubic_coeff_a, out=out,
+                                          workspace=self.ws)
         return self.gs.gs_deform_conv(d["X"], d["W"], d["offset"], d["B"], d["mask"],
                                       kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
                                       dilations=w.dilations, group=w.group,
@@ -295,7 +310,8 @@ def time_e2e(case, steps, warmup):
         def step():
             gs.gs_grid_sample_from_host(pinned["X"], pinned["grid"], case.mode, w.padding_mode,
                                         w.align_corners, w.cubic_coeff_a, out=out_host,
-                                        streamer=streamer)
+                                        streamer=streamer,
+                                        workspace="auto" if case.ws is not None else None)
     else:
         d = {k: torch.empty_like(v, device=case.device) for k, v in case.host.items()}
 
@@ -384,9 +400,13 @@ def workload_desc(case):
                 f"{case.dtype}, out {tuple(w.out_spatial)}, {case.mode}, {w.padding_mode}, "
                 f"align_corners={w.align_corners}")
     if w.kind == "grid_sample":
+        ws = getattr(case, "ws", None)
+        via = (f"; gs_grid_sample_ws, channel-last workspace {ws.numel() / 2**20:.0f} MiB"
+               if ws is not None else "")
         return (f"{case.name}: GridSample {w.r}-D, X {tuple(w.x_shape)} {w.x_dist}, grid "
                 f"({w.x_shape[0]},{','.join(map(str, w.out_spatial))},{w.r}) {w.grid_dist}, "
-                f"{case.dtype}, {case.mode}, {w.padding_mode}, align_corners={w.align_corners}")
+                f"{case.dtype}, {case.mode}, {w.padding_mode}, align_corners={w.align_corners}"
+                f"{via}")
     return (f"{case.name}: DeformConv 2-D, X {tuple(w.x_shape)}, W ({w.oc},{w.x_shape[1]},3,3), "
             f"pads 1, stride 1, offset/mask from N(0,1), {case.dtype}")
 
@@ -411,7 +431,8 @@ def main():
     pk = peaks()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
 
-    case = Case(args.workload, args.dtype, device, args.mode, seed_offset=rank)
+    case = Case(args.workload, args.dtype, device, args.mode, seed_offset=rank,
+                workspace=args.workspace)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         time.sleep(0.6)   # let nvidia-smi start reporting before the timed region
@@ -436,19 +457,25 @@ def main():
 
     extra = []
     if rank == 0 and not args.no_extra:
-        for name, dt, mode in (("stn2d", "bfloat16", None), ("stn3d", "float32", None),
-                               ("gs2d_cubic", "float32", "cubic"), ("gs2d_cubic", "float16", "cubic"),
-                               ("gs2d_cubic", "float32", "nearest"),
-                               ("gs2d_cubic", "float16", "nearest"), ("gs2d_small", "float32", None),
-                               ("deform2d", "float32", None), ("deform2d", "bfloat16", None)):
-            if (name, dt, mode) == (args.workload, args.dtype, args.mode):
+        for name, dt, mode, ws in (
+                ("stn2d", "bfloat16", None, False), ("stn3d", "float32", None, False),
+                ("gs2d_cubic", "float32", "cubic", False), ("gs2d_cubic", "float16", "cubic", False),
+                ("gs2d_cubic", "float32", "nearest", False),
+                ("gs2d_cubic", "float16", "nearest", False),
+                ("gs2d_cubic", "float32", "cubic", True), ("gs2d_cubic", "float16", "cubic", True),
+                ("gs2d_cubic", "float32", "nearest", True),
+                ("gs2d_cubic", "float16", "nearest", True),
+                ("gs2d_small", "float32", None, False),
+                ("deform2d", "float32", None, False), ("deform2d", "bfloat16", None, False)):
+            if (name, dt, mode, ws) == (args.workload, args.dtype, args.mode, args.workspace):
                 continue
-            c2 = Case(name, dt, device, mode)
+            c2 = Case(name, dt, device, mode, workspace=ws)
             st, _, _ = time_steps(c2, args.extra_steps, 5, flush)
             m2 = sum(st) / len(st)
             extra.append({"workload": workload_desc(c2), "dtype": DT_SHORT[dt],
                           "ms_per_step": round(m2, 5), "value": round(c2.outputs / (m2 * 1e-3), 1),
-                          "unit": UNIT, "roofline": roofline_for(c2, m2, pk)})
+                          "unit": UNIT, "kernel": c2.kernel_tag, "launches_per_step": c2.launches,
+                          "roofline": roofline_for(c2, m2, pk)})
             del c2
             torch.cuda.empty_cache()
 
@@ -468,7 +495,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * case.launches,
             "clocks": clocks,
             "kernel": case.kernel_tag,
             "src_sha": kernel_source_sha(case.kernel_tag),

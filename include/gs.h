@@ -104,8 +104,8 @@ gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const voi
 
 /*
  * gs_grid_sample_workspace_size -- device workspace that gs_grid_sample_ws
- * asks for with these shapes: a whole number of channel-last images (at least
- * one, about 32 MB at most).  0 means the call never uses a workspace (rank
+ * asks for with these shapes: a whole number of image slots (at least one,
+ * about 32 MB at most), a slot being (H*W + 1) * C elements of `dt`.  0 means the call never uses a workspace (rank
  * other than 2, C * element size not a multiple of 16 bytes, C*H*W >= 2^31, or
  * an empty tensor).  Arguments as gs_grid_sample; `bytes` is a host output.
  * Shape errors are reported as by gs_grid_sample.
@@ -118,15 +118,16 @@ gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int
  * (GridSample - version 20, as above; the same results, value for value).
  *
  *   workspace        device, 16-byte aligned (GS_ERR_ALIGN), or NULL.
- *   workspace_bytes  its size.  With at least one image's worth (C*H*W
- *                    elements of `dt`), 2-D calls copy X to channel-last order
- *                    there, as many whole images at a time as it holds, and
+ *   workspace_bytes  its size.  With room for one image slot ((H*W + 1) * C
+ *                    elements of `dt`: a zero pixel, then the image), 2-D
+ *                    calls copy X to channel-last order there, as many whole
+ *                    images at a time as it holds, and
  *                    read every tap as 16-byte runs of channels: for grids
  *                    without spatial locality this cuts the bytes read per
  *                    output several fold.  The size that
  *                    gs_grid_sample_workspace_size gives keeps a chunk
  *                    resident in L2; a larger one is allowed but not faster.
- *                    With less than one image, or NULL, it is gs_grid_sample.
+ *                    With less, or NULL, it is gs_grid_sample.
  *
  * The workspace's contents on entry do not matter and are garbage on return.
  * Calls on different streams must not share a workspace while in flight.

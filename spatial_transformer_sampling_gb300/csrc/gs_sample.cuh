@@ -394,7 +394,7 @@ cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleA
         return launch_sample_mode<T, 3, true>(X, src, Y, P, mode, s);
     }
     if (ws && nhwc_workspace_bytes<T>(args, r, affine) > 0 &&
-        ws_bytes >= (size_t)args.C * args.in_plane * sizeof(T))
+        ws_bytes >= nhwc_min_workspace_bytes<T>(args))
         return launch_nhwc<T>(X, src, Y, P, mode, ws, ws_bytes, s);
     if (r == 1) return launch_sample_mode<T, 1, false>(X, src, Y, P, mode, s);
     if (r == 2) return launch_sample_mode<T, 2, false>(X, src, Y, P, mode, s);

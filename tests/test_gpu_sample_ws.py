@@ -76,18 +76,36 @@ def test_workspace_channel_counts(gs_cuda, oracle_mod, dtype, C, mode):
     _check(Y, ref, mode, dtype, f"ws C={C} {mode} {dtype}")
 
 
-@pytest.mark.parametrize("images_per_chunk", [1, 2, 3])
-def test_workspace_chunks(gs_cuda, oracle_mod, images_per_chunk):
-    """A workspace of k images runs ceil(N / k) transpose + sample rounds."""
-    g = wl.rng(40 + images_per_chunk)
+@pytest.mark.parametrize("slots", [1, 2, 3, 4, 5, 6, 12])
+def test_workspace_chunks(gs_cuda, oracle_mod, slots):
+    """One slot: copy and sample alternate image by image.  k >= 2 slots: two
+    buffers of k // 2 images, each launch sampling one chunk while copying the
+    next (5 images: ragged last chunk)."""
+    g = wl.rng(40 + slots)
     xs, out = (5, 32, 17, 15), (20, 19)
     Xt = wl.as_dtype(g.normal(size=xs), "float32")
     Gt = wl.as_dtype(_grid(g, xs[0], out), "float32")
-    img = xs[1] * xs[2] * xs[3] * 4
-    ws = torch.empty(images_per_chunk * img + 8, dtype=torch.uint8, device="cuda")
-    Y = gs_cuda.gs_grid_sample_ws(Xt.cuda(), Gt.cuda(), ws, "cubic", "reflection", 1)
+    slot = xs[1] * (xs[2] * xs[3] + 1) * 4     # a zero pixel, then the image
+    ws = torch.empty(slots * slot + 8, dtype=torch.uint8, device="cuda")
+    Xd, Gd = Xt.cuda(), Gt.cuda()
+    Y = gs_cuda.gs_grid_sample_ws(Xd, Gd, ws, "cubic", "reflection", 1)
     ref = oracle_mod.grid_sample(exact(Xt), exact(Gt), "cubic", "reflection", 1)
-    assert_parity(Y, ref, "float32", f"{images_per_chunk} images per chunk")
+    assert_parity(Y, ref, "float32", f"{slots} slots")
+    assert torch.equal(Y, gs_cuda.gs_grid_sample(Xd, Gd, "cubic", "reflection", 1))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_workspace_small_output_large_input(gs_cuda, oracle_mod, dtype):
+    """Few output positions per image, many copy tiles: each sampling block
+    also copies many tiles of the next chunk."""
+    g = wl.rng(61)
+    xs, out = (4, 16, 64, 70), (5, 7)
+    Xt = wl.as_dtype(g.normal(size=xs), dtype)
+    Gt = wl.as_dtype(_grid(g, xs[0], out), dtype)
+    for ws in ("auto", torch.empty(2 * 16 * (64 * 70 + 1) * 4, dtype=torch.uint8, device="cuda")):
+        Y = gs_cuda.gs_grid_sample_ws(Xt.cuda(), Gt.cuda(), ws, "linear", "zeros", 0)
+        ref = oracle_mod.grid_sample(exact(Xt), exact(Gt), "linear", "zeros", 0)
+        assert_parity(Y, ref, dtype, "small output, large input")
 
 
 def test_workspace_too_small_or_ineligible_takes_the_gather(gs_cuda, oracle_mod):
@@ -101,7 +119,7 @@ def test_workspace_too_small_or_ineligible_takes_the_gather(gs_cuda, oracle_mod)
     assert_parity(Y, ref, "float32", "ineligible C")
     Xt = wl.as_dtype(g.normal(size=(2, 8, 9, 10)), "float32")
     ref = oracle_mod.grid_sample(exact(Xt), exact(Gt), "linear", "zeros", 0)
-    small = torch.empty(8 * 9 * 10 * 4 - 16, dtype=torch.uint8, device="cuda")
+    small = torch.empty(8 * (9 * 10 + 1) * 4 - 16, dtype=torch.uint8, device="cuda")
     Y = gs_cuda.gs_grid_sample_ws(Xt.cuda(), Gt.cuda(), small, "linear", "zeros", 0)
     assert_parity(Y, ref, "float32", "workspace below one image")
     Y = gs_cuda.gs_grid_sample_ws(Xt.cuda(), Gt.cuda(), None, "linear", "zeros", 0)
