@@ -104,11 +104,12 @@ gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const voi
 
 /*
  * gs_grid_sample_workspace_size -- device workspace that gs_grid_sample_ws
- * asks for with these shapes: a whole number of image slots (at least one,
- * about 32 MB at most), a slot being (H*W + 1) * C elements of `dt`.  0 means the call never uses a workspace (rank
- * other than 2, C * element size not a multiple of 16 bytes, C*H*W >= 2^31, or
- * an empty tensor).  Arguments as gs_grid_sample; `bytes` is a host output.
- * Shape errors are reported as by gs_grid_sample.
+ * asks for with these shapes: whole image slots, a slot being (H*W + 1) * C
+ * elements of `dt`, enough for the batch in equal chunks of at most about
+ * 512 MB (at least one slot).  0 means the call never uses a workspace (rank
+ * other than 2, C * element size not a multiple of 16 bytes,
+ * (H*W + 1) * C >= 2^31, or an empty tensor).  Arguments as gs_grid_sample;
+ * `bytes` is a host output.  Shape errors are reported as by gs_grid_sample.
  */
 gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int64_t *out_spatial,
                                         gs_dtype dt, size_t *bytes);
@@ -121,13 +122,12 @@ gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int
  *   workspace_bytes  its size.  With room for one image slot ((H*W + 1) * C
  *                    elements of `dt`: a zero pixel, then the image), 2-D
  *                    calls copy X to channel-last order there, as many whole
- *                    images at a time as it holds, and
- *                    read every tap as 16-byte runs of channels: for grids
- *                    without spatial locality this cuts the bytes read per
- *                    output several fold.  The size that
- *                    gs_grid_sample_workspace_size gives keeps a chunk
- *                    resident in L2; a larger one is allowed but not faster.
- *                    With less, or NULL, it is gs_grid_sample.
+ *                    images at a time as it holds, then read every tap as
+ *                    16-byte runs of channels: for grids without spatial
+ *                    locality this cuts the bytes read per output several
+ *                    fold.  Each chunk costs a copy launch and a sampling
+ *                    launch, so fewer, larger chunks are faster.  With less
+ *                    than one slot, or NULL, it is gs_grid_sample.
  *
  * The workspace's contents on entry do not matter and are garbage on return.
  * Calls on different streams must not share a workspace while in flight.
