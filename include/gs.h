@@ -13,8 +13,9 @@
  *  - The library allocates no memory, keeps no state between calls and never
  *    synchronises: every call only enqueues kernels on `stream` (0 = the
  *    legacy default stream) and returns.  Scratch space, where a path uses
- *    some, is a workspace the caller passes in.  Output buffers must not
- *    overlap inputs.
+ *    some, is a workspace the caller passes in, or (gs_grid_sample_static) a
+ *    fixed array in the library's static device memory.  Output buffers must
+ *    not overlap inputs.
  *  - Arguments are checked on the host before anything is enqueued; a bad
  *    argument returns its gs_status and leaves the outputs untouched.  A
  *    failed launch returns GS_ERR_CUDA.  A tensor with a zero extent is valid
@@ -136,6 +137,35 @@ gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const 
                             const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
                             int align_corners, float cubic_coeff_a, void *workspace,
                             size_t workspace_bytes, void *Y, cudaStream_t stream);
+
+/* Size of the scratch gs_grid_sample_static uses: 64 MiB per device. */
+#define GS_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/*
+ * gs_grid_sample_static -- gs_grid_sample_ws whose workspace is a fixed
+ * GS_STATIC_WORKSPACE_BYTES array in the library's static device memory, so
+ * the call allocates nothing (no cudaMalloc, no allocating library call) and
+ * needs no caller buffer: for callers that may not allocate, such as code
+ * being captured into a CUDA graph.  The operator pages have no counterpart
+ * to this call; it is a deployment convenience around the same kernels.
+ *
+ *   Arguments, results and errors as gs_grid_sample.  A call the channel-
+ *   last path takes (see gs_grid_sample_workspace_size) whose image slot,
+ *   (H*W + 1) * C elements of `dt`, exceeds GS_STATIC_WORKSPACE_BYTES
+ *   returns GS_ERR_SHAPE before anything is enqueued; other calls run the
+ *   NCHW gather and touch no scratch.
+ *
+ * The scratch needs no clearing: each call writes every byte it reads.  The
+ * first call on each device looks up the scratch's address (and the error
+ * word's) once with cudaGetSymbolAddress, GS_ERR_CUDA if that fails: make it
+ * before any stream capture.  There is one scratch per device and process:
+ * calls in flight at the same time on different streams, or from different
+ * host threads, race on it and corrupt each other's results.
+ */
+gs_status gs_grid_sample_static(const void *X, const int64_t *x_shape, int r, const void *grid,
+                                const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                                int align_corners, float cubic_coeff_a, void *Y,
+                                cudaStream_t stream);
 
 /*
  * gs_affine_sample -- GridSample(X, AffineGrid(theta, size)) in one kernel:

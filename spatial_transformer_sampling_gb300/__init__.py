@@ -73,6 +73,7 @@ def load_library(path=None):
     L.gs_grid_sample_workspace_size.argtypes = [i64p, ci, i64p, ci, ctypes.POINTER(ctypes.c_size_t)]
     L.gs_grid_sample_ws.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, ctypes.c_size_t,
                                     vp, vp]
+    L.gs_grid_sample_static.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
     L.gs_affine_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
     L.gs_deform_conv.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
                                  ctypes.POINTER(DeformAttrs), ci, vp, vp]
@@ -81,7 +82,8 @@ def load_library(path=None):
     L.gs_device_status.argtypes = [vp]
     L.gs_version.restype = ctypes.c_char_p
     for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
-              "gs_grid_sample_ws", "gs_affine_sample", "gs_deform_conv", "gs_device_status"):
+              "gs_grid_sample_ws", "gs_grid_sample_static", "gs_affine_sample", "gs_deform_conv",
+              "gs_device_status"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -210,6 +212,27 @@ def gs_grid_sample_ws(X, grid, workspace="auto", mode="linear", padding_mode="ze
                                          int(align_corners), float(cubic_coeff_a), ws_ptr,
                                          ws_bytes, _ptr(out), _stream(X)), "gs_grid_sample_ws")
     return out
+
+
+def gs_grid_sample_static(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
+                          cubic_coeff_a=-0.75, out=None):
+    """gs_grid_sample with the library's static scratch (see gs_grid_sample_static in
+    gs.h): no allocation in the call; concurrent calls race on the one scratch."""
+    torch = _torch()
+    _check_tensors(X, grid, out)
+    r = X.dim() - 2
+    out_sp = list(grid.shape[1:-1])
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
+    _ok(load_library().gs_grid_sample_static(_ptr(X), _i64(X.shape), r, _ptr(grid),
+                                             _i64(out_sp), _dtype_code(X), MODES[mode],
+                                             PADS[padding_mode], int(align_corners),
+                                             float(cubic_coeff_a), _ptr(out), _stream(X)),
+        "gs_grid_sample_static")
+    return out
+
+
+STATIC_WORKSPACE_BYTES = 64 << 20   # GS_STATIC_WORKSPACE_BYTES in gs.h
 
 
 def gs_affine_sample(theta, size, X, mode="linear", padding_mode="zeros", align_corners=0,

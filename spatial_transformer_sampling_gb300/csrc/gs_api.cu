@@ -12,6 +12,12 @@
 // gs_device_status reads and clears it.
 __device__ unsigned g_gs_error_word = 0;
 
+// Scratch of gs_grid_sample_static: GS_STATIC_WORKSPACE_BYTES per device in
+// the module's static device memory, so the call allocates nothing.  Nothing
+// in it needs to start at zero: each call's copy kernel writes every byte the
+// sampler then reads, the zero pixels included.
+static __device__ __align__(256) unsigned char g_gs_static_ws[GS_STATIC_WORKSPACE_BYTES];
+
 namespace {
 
 // Device address of g_gs_error_word on the current device (looked up once per
@@ -24,6 +30,20 @@ unsigned *error_word() {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_gs_error_word) != cudaSuccess) return nullptr;
         cache[dev] = (unsigned *)p;
+    }
+    return cache[dev];
+}
+
+// Device address of g_gs_static_ws on the current device, looked up once per
+// device (nullptr if the lookup fails).
+void *static_workspace() {
+    static void *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gs_static_ws) != cudaSuccess) return nullptr;
+        cache[dev] = p;
     }
     return cache[dev];
 }
@@ -197,6 +217,48 @@ gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const 
     return dispatch(dt, [&](auto tag) {
         return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, workspace,
                                                 workspace_bytes, stream);
+    });
+}
+
+gs_status gs_grid_sample_static(const void *X, const int64_t *x_shape, int r, const void *grid,
+                                const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
+                                int align_corners, float cubic_coeff_a, void *Y,
+                                cudaStream_t stream) {
+    if (r < 1 || r > 3) return GS_ERR_RANK;
+    gs::SampleArgs args;
+    bool skip = false;
+    gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,
+                                cubic_coeff_a, Y, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    if (!grid) return GS_ERR_NULL;
+    if (!aligned(grid, elem_size(dt))) return GS_ERR_ALIGN;
+    size_t need = 0, slot = 0;   // asked-for size; one image slot (the least it runs with)
+    switch (dt) {
+        case GS_F32:
+            need = gs::sample_workspace_bytes<float>(args, r, false);
+            slot = gs::sample_min_workspace_bytes<float>(args);
+            break;
+        case GS_F16:
+            need = gs::sample_workspace_bytes<__half>(args, r, false);
+            slot = gs::sample_min_workspace_bytes<__half>(args);
+            break;
+        default:
+            need = gs::sample_workspace_bytes<__nv_bfloat16>(args, r, false);
+            slot = gs::sample_min_workspace_bytes<__nv_bfloat16>(args);
+            break;
+    }
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    if (need > 0) {   // the channel-last path takes this call
+        if (slot > (size_t)GS_STATIC_WORKSPACE_BYTES) return GS_ERR_SHAPE;
+        ws = static_workspace();
+        if (!ws) return GS_ERR_CUDA;
+        ws_bytes = (size_t)GS_STATIC_WORKSPACE_BYTES;
+    }
+    args.err = error_word();
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_sample<decltype(tag)>(X, grid, Y, args, r, (int)mode, false, ws, ws_bytes,
+                                                stream);
     });
 }
 

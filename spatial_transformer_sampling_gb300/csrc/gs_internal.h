@@ -47,9 +47,12 @@ struct DeformArgs {
 template <typename T>
 cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
                           int mode, bool affine, void *ws, size_t ws_bytes, cudaStream_t s);
-// Workspace bytes the channel-last path asks for (0: this call never takes it).
+// Workspace bytes the channel-last path asks for (0: this call never takes it),
+// and the least it runs with (one image slot).
 template <typename T>
 size_t sample_workspace_bytes(const SampleArgs &args, int r, bool affine);
+template <typename T>
+size_t sample_min_workspace_bytes(const SampleArgs &args);
 template <typename T>
 cudaError_t launch_affine_grid(const void *theta, void *grid, const AffineGridArgs &args, int r,
                                cudaStream_t s);

@@ -7,6 +7,7 @@ namespace gs {
 template cudaError_t launch_sample<__nv_bfloat16>(const void *, const void *, void *, const SampleArgs &,
                                           int, int, bool, void *, size_t, cudaStream_t);
 template size_t sample_workspace_bytes<__nv_bfloat16>(const SampleArgs &, int, bool);
+template size_t sample_min_workspace_bytes<__nv_bfloat16>(const SampleArgs &);
 template cudaError_t launch_affine_grid<__nv_bfloat16>(const void *, void *, const AffineGridArgs &, int,
                                                cudaStream_t);
 template cudaError_t launch_deform<__nv_bfloat16>(const void *, const void *, const void *, const void *,

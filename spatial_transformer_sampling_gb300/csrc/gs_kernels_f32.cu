@@ -7,6 +7,7 @@ namespace gs {
 template cudaError_t launch_sample<float>(const void *, const void *, void *, const SampleArgs &,
                                           int, int, bool, void *, size_t, cudaStream_t);
 template size_t sample_workspace_bytes<float>(const SampleArgs &, int, bool);
+template size_t sample_min_workspace_bytes<float>(const SampleArgs &);
 template cudaError_t launch_affine_grid<float>(const void *, void *, const AffineGridArgs &, int,
                                                cudaStream_t);
 template cudaError_t launch_deform<float>(const void *, const void *, const void *, const void *,

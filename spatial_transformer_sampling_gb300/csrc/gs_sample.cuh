@@ -386,6 +386,11 @@ size_t sample_workspace_bytes(const SampleArgs &args, int r, bool affine) {
 }
 
 template <typename T>
+size_t sample_min_workspace_bytes(const SampleArgs &args) {
+    return nhwc_min_workspace_bytes<T>(args);
+}
+
+template <typename T>
 cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleArgs &args, int r,
                           int mode, bool affine, void *ws, size_t ws_bytes, cudaStream_t s) {
     const SampleParams P = make_params<T>(args, r);

@@ -51,8 +51,15 @@ def _i64(v):
 FAKE = 0x10000   # a non-null, aligned pointer value; never dereferenced on these paths
 
 
-def _gsample(L, x_shape, out, r=2, dt=0, mode=0, pad=0, ac=0, a=-0.75, X=FAKE, grid=FAKE, Y=FAKE):
-    return L.gs_grid_sample(X, _i64(x_shape), r, grid, _i64(out), dt, mode, pad, ac, a, Y, None)
+def _gsample(L, x_shape, out, r=2, dt=0, mode=0, pad=0, ac=0, a=-0.75, X=FAKE, grid=FAKE, Y=FAKE,
+             entry="gs_grid_sample"):
+    if entry == "gs_grid_sample_ws":   # no workspace: checks as gs_grid_sample
+        return L.gs_grid_sample_ws(X, _i64(x_shape), r, grid, _i64(out), dt, mode, pad, ac, a,
+                                   None, 0, Y, None)
+    return getattr(L, entry)(X, _i64(x_shape), r, grid, _i64(out), dt, mode, pad, ac, a, Y, None)
+
+
+ENTRIES = ["gs_grid_sample", "gs_grid_sample_ws", "gs_grid_sample_static"]
 
 
 @pytest.mark.parametrize("kwargs,status", [
@@ -64,16 +71,23 @@ def _gsample(L, x_shape, out, r=2, dt=0, mode=0, pad=0, ac=0, a=-0.75, X=FAKE, g
     (dict(x_shape=[1, 1, 1 << 16, 1 << 16]), 3), (dict(x_shape=[1, 1, 0, 4]), 3),
     (dict(mode=2, a=float("nan")), 5),
 ])
-def test_grid_sample_rejects_bad_arguments(L, kwargs, status):
-    args = dict(x_shape=[2, 3, 4, 5], out=[3, 3])
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_grid_sample_rejects_bad_arguments(L, kwargs, status, entry):
+    args = dict(x_shape=[2, 3, 4, 5], out=[3, 3], entry=entry)
     args.update(kwargs)
     assert _gsample(L, **args) == status
 
 
 @pytest.mark.parametrize("x_shape,out", [([0, 3, 4, 5], [3, 3]), ([2, 0, 4, 5], [3, 3]),
                                          ([2, 3, 4, 5], [0, 3])])
-def test_empty_tensors_return_ok_without_a_launch(L, x_shape, out):
-    assert _gsample(L, x_shape, out, X=None, grid=None, Y=None) == 0
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_empty_tensors_return_ok_without_a_launch(L, x_shape, out, entry):
+    assert _gsample(L, x_shape, out, X=None, grid=None, Y=None, entry=entry) == 0
+
+
+def test_static_scratch_rejects_an_image_slot_beyond_its_size(L):
+    # (512*513 + 1) * 64 fp32 elements exceed the 64 MiB scratch: refused on the host
+    assert _gsample(L, [1, 64, 512, 513], [4, 4], entry="gs_grid_sample_static") == 3
 
 
 def test_affine_sample_checks(L):
