@@ -84,7 +84,9 @@ KERNEL_SOURCES = {
     "band_kernel": ["gs_band.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "sample_kernel": ["gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "nhwc_sample_kernel": ["gs_nhwc.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_internal.h"],
-    "deform": ["gs_deform.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "deform": ["gs_deform.cuh", "gs_deform_tc.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "deform_tc_nhwc": ["gs_deform_tc.cuh", "gs_copy.cuh", "gs_common.cuh", "gs_ptx.cuh",
+                       "gs_internal.h"],
 }
 
 
@@ -223,6 +225,14 @@ class Case:
             self.outputs = N * w.oc * oH * oW
             self.flops = 2.0 * N * oH * oW * w.oc * (C // w.group) * w.kernel[0] * w.kernel[1]
             self.kernel_tag = f"deform<{DT_SHORT[dtype]}>"
+            if workspace:
+                a = gs.deform_attrs(w.kernel, w.pads, w.strides, w.dilations, w.group,
+                                    w.offset_group)
+                nbytes = gs.gs_deform_conv_workspace_size(w.x_shape, w.oc, a, getattr(torch, dtype))
+                if nbytes:
+                    self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+                    self.launches = 3   # pack W, copy X, sample + contract
+                    self.kernel_tag = f"deform_tc_nhwc<{DT_SHORT[dtype]}>"
         self.dev = {k: v.to(device) for k, v in self.host.items()}
         self.out = torch.empty(self._out_shape(), dtype=self.dev["X"].dtype, device=device)
         # algorithmic bytes: every input read once, the output written once
@@ -252,7 +262,7 @@ class Case:
         return self.gs.gs_deform_conv(d["X"], d["W"], d["offset"], d["B"], d["mask"],
                                       kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
                                       dilations=w.dilations, group=w.group,
-                                      offset_group=w.offset_group, out=out)
+                                      offset_group=w.offset_group, out=out, workspace=self.ws)
 
 
 def flush_l2(buf):
@@ -407,8 +417,11 @@ def workload_desc(case):
                 f"({w.x_shape[0]},{','.join(map(str, w.out_spatial))},{w.r}) {w.grid_dist}, "
                 f"{case.dtype}, {case.mode}, {w.padding_mode}, align_corners={w.align_corners}"
                 f"{via}")
+    ws = getattr(case, "ws", None)
+    via = (f"; gs_deform_conv_ws, channel-last workspace {ws.numel() / 2**20:.1f} MiB"
+           if ws is not None else "")
     return (f"{case.name}: DeformConv 2-D, X {tuple(w.x_shape)}, W ({w.oc},{w.x_shape[1]},3,3), "
-            f"pads 1, stride 1, offset/mask from N(0,1), {case.dtype}")
+            f"pads 1, stride 1, offset/mask from N(0,1), {case.dtype}{via}")
 
 
 def main():
@@ -466,7 +479,8 @@ def main():
                 ("gs2d_cubic", "float32", "nearest", True),
                 ("gs2d_cubic", "float16", "nearest", True),
                 ("gs2d_small", "float32", None, False),
-                ("deform2d", "float32", None, False), ("deform2d", "bfloat16", None, False)):
+                ("deform2d", "float32", None, False), ("deform2d", "bfloat16", None, False),
+                ("deform2d", "bfloat16", None, True)):
             if (name, dt, mode, ws) == (args.workload, args.dtype, args.mode, args.workspace):
                 continue
             c2 = Case(name, dt, device, mode, workspace=ws)

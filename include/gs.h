@@ -225,6 +225,37 @@ gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, i
                          const gs_deform_attrs *attrs, gs_dtype dt, void *Y,
                          cudaStream_t stream);
 
+/*
+ * gs_deform_conv_workspace_size -- device workspace gs_deform_conv_ws asks
+ * for: the packed W (rounded up to 256 bytes) and one channel-last slot of
+ * (H*W + 1) * C elements per image.  0 means the call never uses a
+ * workspace: fp32, or a shape outside the tensor-core path (group or
+ * offset_group > 1, C or oC not a multiple of 16, oC > 256, or W too large
+ * for shared memory).  Arguments as gs_deform_conv (no tensors needed);
+ * `bytes` is a host output.
+ */
+gs_status gs_deform_conv_workspace_size(const int64_t *x_shape, int64_t oC,
+                                        const gs_deform_attrs *attrs, gs_dtype dt, size_t *bytes);
+
+/*
+ * gs_deform_conv_ws -- gs_deform_conv with a caller-owned device workspace
+ * (DeformConv, as above; the same values).
+ *
+ *   workspace        device, 256-byte aligned (GS_ERR_ALIGN), or NULL.
+ *   workspace_bytes  its size.  With room for the packed W and at least one
+ *                    image slot, fp16/bf16 calls on the tensor-core path pack
+ *                    W once, copy X to channel-last order (as many images at a
+ *                    time as it holds) and read each bilinear tap as 16-byte
+ *                    runs of channels.  Otherwise it is gs_deform_conv.
+ *
+ * The workspace's contents on entry do not matter and are garbage on return.
+ * Calls on different streams must not share a workspace while in flight.
+ */
+gs_status gs_deform_conv_ws(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
+                            const void *offset, const void *B, const void *mask,
+                            const gs_deform_attrs *attrs, gs_dtype dt, void *workspace,
+                            size_t workspace_bytes, void *Y, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gs_status_str(gs_status s);
 

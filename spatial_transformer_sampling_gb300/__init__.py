@@ -77,13 +77,17 @@ def load_library(path=None):
     L.gs_affine_sample.argtypes = [vp, i64p, ci, vp, i64p, ci, ci, ci, ci, cf, vp, vp]
     L.gs_deform_conv.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
                                  ctypes.POINTER(DeformAttrs), ci, vp, vp]
+    L.gs_deform_conv_workspace_size.argtypes = [i64p, ctypes.c_int64, ctypes.POINTER(DeformAttrs),
+                                                ci, ctypes.POINTER(ctypes.c_size_t)]
+    L.gs_deform_conv_ws.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
+                                    ctypes.POINTER(DeformAttrs), ci, vp, ctypes.c_size_t, vp, vp]
     L.gs_status_str.argtypes = [ci]
     L.gs_status_str.restype = ctypes.c_char_p
     L.gs_device_status.argtypes = [vp]
     L.gs_version.restype = ctypes.c_char_p
     for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
               "gs_grid_sample_ws", "gs_grid_sample_static", "gs_affine_sample", "gs_deform_conv",
-              "gs_device_status"):
+              "gs_deform_conv_workspace_size", "gs_deform_conv_ws", "gs_device_status"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -269,8 +273,12 @@ def deform_out_hw(H, W, a):
 
 
 def gs_deform_conv(X, W, offset, B=None, mask=None, kernel_shape=None, pads=None, strides=None,
-                   dilations=None, group=1, offset_group=1, out=None):
-    """DeformConv 2-D: X (N,C,H,W), W (oC,C/group,kH,kW), offset (N,og*kH*kW*2,oH,oW)."""
+                   dilations=None, group=1, offset_group=1, out=None, workspace=None):
+    """DeformConv 2-D: X (N,C,H,W), W (oC,C/group,kH,kW), offset (N,og*kH*kW*2,oH,oW).
+
+    ``workspace``: None calls gs_deform_conv; a device tensor (raw bytes) or
+    "auto" (the size gs_deform_conv_workspace_size asks for, from torch's
+    allocator) calls gs_deform_conv_ws."""
     torch = _torch()
     _check_tensors(X, W, offset, B, mask, out)
     a = deform_attrs(kernel_shape if kernel_shape is not None else W.shape[2:], pads, strides,
@@ -278,10 +286,44 @@ def gs_deform_conv(X, W, offset, B=None, mask=None, kernel_shape=None, pads=None
     oH, oW = deform_out_hw(X.shape[2], X.shape[3], a)
     if out is None:
         out = torch.empty((X.shape[0], W.shape[0], oH, oW), dtype=X.dtype, device=X.device)
-    _ok(load_library().gs_deform_conv(_ptr(X), _i64(X.shape), _ptr(W), int(W.shape[0]),
-                                      _ptr(offset), _ptr(B), _ptr(mask), ctypes.byref(a),
-                                      _dtype_code(X), _ptr(out), _stream(X)), "gs_deform_conv")
+    L = load_library()
+    if workspace is None:
+        _ok(L.gs_deform_conv(_ptr(X), _i64(X.shape), _ptr(W), int(W.shape[0]), _ptr(offset),
+                             _ptr(B), _ptr(mask), ctypes.byref(a), _dtype_code(X), _ptr(out),
+                             _stream(X)), "gs_deform_conv")
+        return out
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError(f"workspace must be a tensor, None or 'auto', not {workspace!r}")
+        nbytes = gs_deform_conv_workspace_size(X.shape, int(W.shape[0]), a, X.dtype)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=X.device) if nbytes else None
+    if workspace is not None:
+        if not workspace.is_cuda or workspace.device != X.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on X's device")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    else:
+        ws_ptr, ws_bytes = None, 0
+    _ok(L.gs_deform_conv_ws(_ptr(X), _i64(X.shape), _ptr(W), int(W.shape[0]), _ptr(offset),
+                            _ptr(B), _ptr(mask), ctypes.byref(a), _dtype_code(X), ws_ptr, ws_bytes,
+                            _ptr(out), _stream(X)), "gs_deform_conv_ws")
     return out
+
+
+def gs_deform_conv_workspace_size(x_shape, oC, attrs, dtype):
+    """Workspace bytes gs_deform_conv_ws asks for (0: the call never uses one).
+    ``attrs`` is a DeformAttrs (see deform_attrs)."""
+    torch = _torch()
+    code = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[dtype]
+    n = ctypes.c_size_t(0)
+    _ok(load_library().gs_deform_conv_workspace_size(_i64(x_shape), int(oC), ctypes.byref(attrs),
+                                                     code, ctypes.byref(n)),
+        "gs_deform_conv_workspace_size")
+    return int(n.value)
+
+
+def gs_deform_conv_ws(X, W, offset, B=None, mask=None, workspace="auto", **kw):
+    """gs_deform_conv with a device workspace (see gs_deform_conv_ws in gs.h)."""
+    return gs_deform_conv(X, W, offset, B, mask, workspace=workspace, **kw)
 
 
 def gs_device_status(device=None):

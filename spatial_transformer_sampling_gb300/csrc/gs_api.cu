@@ -134,6 +134,60 @@ gs_status check_sample(const void *X, const int64_t *x_shape, int r, const int64
 
 }  // namespace
 
+namespace {
+
+// Checks of gs_deform_conv; fills *a (err unset) or sets *skip for an empty output.
+gs_status check_deform(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
+                       const void *offset, const void *B, const void *mask,
+                       const gs_deform_attrs *at, gs_dtype dt, const void *Y, bool shapes_only,
+                       gs::DeformArgs *a, bool *skip) {
+    *skip = false;
+    if (!x_shape || !at) return GS_ERR_NULL;
+    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
+    const int64_t N = x_shape[0], C = x_shape[1], H = x_shape[2], Wd = x_shape[3];
+    if (!nc_ok(N, C) || oC < 0 || oC > kMaxSlab) return GS_ERR_SHAPE;
+    if (H < 0 || Wd < 0 || H > kMaxExtent || Wd > kMaxExtent || H * Wd > kMaxSlab)
+        return GS_ERR_SHAPE;
+    for (int i = 0; i < 2; ++i) {
+        if (at->kernel[i] < 1 || at->kernel[i] > 64) return GS_ERR_ATTR;
+        if (at->strides[i] < 1 || at->dilations[i] < 1) return GS_ERR_ATTR;
+        if (at->strides[i] > kMaxExtent || at->dilations[i] > kMaxExtent) return GS_ERR_ATTR;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (at->pads[i] < 0 || at->pads[i] > kMaxExtent) return GS_ERR_ATTR;
+    if (at->group < 1 || at->offset_group < 1) return GS_ERR_ATTR;
+    if (C % at->group || oC % at->group || C % at->offset_group) return GS_ERR_ATTR;
+    const int64_t kH = at->kernel[0], kW = at->kernel[1];
+    const int64_t oH = (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1) / at->strides[0] + 1;
+    const int64_t oW = (Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1) / at->strides[1] + 1;
+    if (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1 < 0 ||
+        Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1 < 0)
+        return GS_ERR_SHAPE;
+    if (oH * oW > kMaxSlab) return GS_ERR_SHAPE;
+    if (N == 0 || oC == 0 || oH == 0 || oW == 0) {
+        *skip = true;
+        return GS_OK;
+    }
+    if (C == 0 || H == 0 || Wd == 0) return GS_ERR_SHAPE;
+    a->N = (int)N; a->C = (int)C; a->H = (int)H; a->W = (int)Wd; a->oC = (int)oC;
+    a->oH = (int)oH; a->oW = (int)oW; a->kH = (int)kH; a->kW = (int)kW;
+    a->pad_t = (int)at->pads[0]; a->pad_l = (int)at->pads[1];
+    a->sH = (int)at->strides[0]; a->sW = (int)at->strides[1];
+    a->dH = (int)at->dilations[0]; a->dW = (int)at->dilations[1];
+    a->group = (int)at->group; a->offset_group = (int)at->offset_group;
+    a->has_bias = B != nullptr; a->has_mask = mask != nullptr;
+    a->err = nullptr;
+    if (shapes_only) return GS_OK;
+    if (!X || !W || !offset || !Y) return GS_ERR_NULL;
+    const size_t es = elem_size(dt);
+    if (!aligned(X, es) || !aligned(W, es) || !aligned(offset, es) || !aligned(Y, es) ||
+        (B && !aligned(B, es)) || (mask && !aligned(mask, es)))
+        return GS_ERR_ALIGN;
+    return GS_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *size,
@@ -286,46 +340,49 @@ gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const 
 gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
                          const void *offset, const void *B, const void *mask,
                          const gs_deform_attrs *at, gs_dtype dt, void *Y, cudaStream_t stream) {
-    if (!x_shape || !at) return GS_ERR_NULL;
-    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
-    const int64_t N = x_shape[0], C = x_shape[1], H = x_shape[2], Wd = x_shape[3];
-    if (!nc_ok(N, C) || oC < 0 || oC > kMaxSlab) return GS_ERR_SHAPE;
-    if (H < 0 || Wd < 0 || H > kMaxExtent || Wd > kMaxExtent || H * Wd > kMaxSlab)
-        return GS_ERR_SHAPE;
-    for (int i = 0; i < 2; ++i) {
-        if (at->kernel[i] < 1 || at->kernel[i] > 64) return GS_ERR_ATTR;
-        if (at->strides[i] < 1 || at->dilations[i] < 1) return GS_ERR_ATTR;
-        if (at->strides[i] > kMaxExtent || at->dilations[i] > kMaxExtent) return GS_ERR_ATTR;
-    }
-    for (int i = 0; i < 4; ++i)
-        if (at->pads[i] < 0 || at->pads[i] > kMaxExtent) return GS_ERR_ATTR;
-    if (at->group < 1 || at->offset_group < 1) return GS_ERR_ATTR;
-    if (C % at->group || oC % at->group || C % at->offset_group) return GS_ERR_ATTR;
-    const int64_t kH = at->kernel[0], kW = at->kernel[1];
-    const int64_t oH = (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1) / at->strides[0] + 1;
-    const int64_t oW = (Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1) / at->strides[1] + 1;
-    if (H + at->pads[0] + at->pads[2] - at->dilations[0] * (kH - 1) - 1 < 0 ||
-        Wd + at->pads[1] + at->pads[3] - at->dilations[1] * (kW - 1) - 1 < 0)
-        return GS_ERR_SHAPE;
-    if (oH * oW > kMaxSlab) return GS_ERR_SHAPE;
-    if (N == 0 || oC == 0 || oH == 0 || oW == 0) return GS_OK;
-    if (C == 0 || H == 0 || Wd == 0) return GS_ERR_SHAPE;
-    if (!X || !W || !offset || !Y) return GS_ERR_NULL;
-    const size_t es = elem_size(dt);
-    if (!aligned(X, es) || !aligned(W, es) || !aligned(offset, es) || !aligned(Y, es) ||
-        (B && !aligned(B, es)) || (mask && !aligned(mask, es)))
-        return GS_ERR_ALIGN;
     gs::DeformArgs a;
-    a.N = (int)N; a.C = (int)C; a.H = (int)H; a.W = (int)Wd; a.oC = (int)oC;
-    a.oH = (int)oH; a.oW = (int)oW; a.kH = (int)kH; a.kW = (int)kW;
-    a.pad_t = (int)at->pads[0]; a.pad_l = (int)at->pads[1];
-    a.sH = (int)at->strides[0]; a.sW = (int)at->strides[1];
-    a.dH = (int)at->dilations[0]; a.dW = (int)at->dilations[1];
-    a.group = (int)at->group; a.offset_group = (int)at->offset_group;
-    a.has_bias = B != nullptr; a.has_mask = mask != nullptr;
+    bool skip = false;
+    const gs_status st = check_deform(X, x_shape, W, oC, offset, B, mask, at, dt, Y, false, &a, &skip);
+    if (st != GS_OK || skip) return st;
     a.err = error_word();
     return dispatch(dt, [&](auto tag) {
         return gs::launch_deform<decltype(tag)>(X, W, offset, B, mask, Y, a, stream);
+    });
+}
+
+gs_status gs_deform_conv_workspace_size(const int64_t *x_shape, int64_t oC,
+                                        const gs_deform_attrs *attrs, gs_dtype dt, size_t *bytes) {
+    if (!bytes) return GS_ERR_NULL;
+    *bytes = 0;
+    gs::DeformArgs a;
+    bool skip = false;
+    const gs_status st = check_deform(nullptr, x_shape, nullptr, oC, nullptr, nullptr, nullptr,
+                                      attrs, dt, nullptr, true, &a, &skip);
+    if (st != GS_OK || skip) return st;
+    a.has_bias = 1;
+    a.has_mask = 1;
+    switch (dt) {
+        case GS_F32: *bytes = gs::deform_ws_bytes<float>(a); break;
+        case GS_F16: *bytes = gs::deform_ws_bytes<__half>(a); break;
+        default: *bytes = gs::deform_ws_bytes<__nv_bfloat16>(a); break;
+    }
+    return GS_OK;
+}
+
+gs_status gs_deform_conv_ws(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
+                            const void *offset, const void *B, const void *mask,
+                            const gs_deform_attrs *at, gs_dtype dt, void *workspace,
+                            size_t workspace_bytes, void *Y, cudaStream_t stream) {
+    gs::DeformArgs a;
+    bool skip = false;
+    const gs_status st = check_deform(X, x_shape, W, oC, offset, B, mask, at, dt, Y, false, &a, &skip);
+    if (st != GS_OK || skip) return st;
+    if (workspace && !aligned(workspace, 256)) return GS_ERR_ALIGN;
+    if (workspace_bytes && !workspace) return GS_ERR_NULL;
+    a.err = error_word();
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_deform_ws<decltype(tag)>(X, W, offset, B, mask, Y, a, workspace,
+                                                   workspace_bytes, stream);
     });
 }
 

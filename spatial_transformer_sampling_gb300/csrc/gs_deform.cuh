@@ -198,4 +198,22 @@ cudaError_t launch_deform(const void *X, const void *W, const void *offset, cons
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_deform_ws(const void *X, const void *W, const void *offset, const void *B,
+                             const void *mask, void *Y, const DeformArgs &a, void *ws,
+                             size_t ws_bytes, cudaStream_t s) {
+    if constexpr (!std::is_same<T, float>::value) {
+        bool used = false;
+        const cudaError_t e = launch_deform_tc_ws<T>(X, W, offset, B, mask, Y, a, ws, ws_bytes, s,
+                                                     &used);
+        if (used || e != cudaSuccess) return e;
+    }
+    return launch_deform<T>(X, W, offset, B, mask, Y, a, s);
+}
+
+template <typename T>
+size_t deform_ws_bytes(const DeformArgs &a) {
+    return deform_workspace_bytes<T>(a);
+}
+
 }  // namespace gs

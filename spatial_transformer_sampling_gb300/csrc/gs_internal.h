@@ -59,5 +59,14 @@ cudaError_t launch_affine_grid(const void *theta, void *grid, const AffineGridAr
 template <typename T>
 cudaError_t launch_deform(const void *X, const void *W, const void *offset, const void *B,
                           const void *mask, void *Y, const DeformArgs &args, cudaStream_t s);
+// DeformConv with an optional workspace for the channel-last tensor-core path
+// (too small or NULL: launch_deform), and the workspace bytes that path asks
+// for (0: it never takes the shape).
+template <typename T>
+cudaError_t launch_deform_ws(const void *X, const void *W, const void *offset, const void *B,
+                             const void *mask, void *Y, const DeformArgs &args, void *ws,
+                             size_t ws_bytes, cudaStream_t s);
+template <typename T>
+size_t deform_ws_bytes(const DeformArgs &args);
 
 }  // namespace gs

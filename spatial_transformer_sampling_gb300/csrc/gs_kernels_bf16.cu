@@ -12,4 +12,8 @@ template cudaError_t launch_affine_grid<__nv_bfloat16>(const void *, void *, con
                                                cudaStream_t);
 template cudaError_t launch_deform<__nv_bfloat16>(const void *, const void *, const void *, const void *,
                                           const void *, void *, const DeformArgs &, cudaStream_t);
+template cudaError_t launch_deform_ws<__nv_bfloat16>(const void *, const void *, const void *, const void *,
+                                             const void *, void *, const DeformArgs &, void *,
+                                             size_t, cudaStream_t);
+template size_t deform_ws_bytes<__nv_bfloat16>(const DeformArgs &);
 }  // namespace gs

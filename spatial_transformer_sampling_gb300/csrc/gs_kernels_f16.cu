@@ -12,4 +12,8 @@ template cudaError_t launch_affine_grid<__half>(const void *, void *, const Affi
                                                cudaStream_t);
 template cudaError_t launch_deform<__half>(const void *, const void *, const void *, const void *,
                                           const void *, void *, const DeformArgs &, cudaStream_t);
+template cudaError_t launch_deform_ws<__half>(const void *, const void *, const void *, const void *,
+                                             const void *, void *, const DeformArgs &, void *,
+                                             size_t, cudaStream_t);
+template size_t deform_ws_bytes<__half>(const DeformArgs &);
 }  // namespace gs

@@ -12,4 +12,8 @@ template cudaError_t launch_affine_grid<float>(const void *, void *, const Affin
                                                cudaStream_t);
 template cudaError_t launch_deform<float>(const void *, const void *, const void *, const void *,
                                           const void *, void *, const DeformArgs &, cudaStream_t);
+template cudaError_t launch_deform_ws<float>(const void *, const void *, const void *, const void *,
+                                             const void *, void *, const DeformArgs &, void *,
+                                             size_t, cudaStream_t);
+template size_t deform_ws_bytes<float>(const DeformArgs &);
 }  // namespace gs

@@ -30,52 +30,15 @@
 #include <cstring>
 #include <type_traits>
 
+#include "gs_copy.cuh"
+
 namespace gs {
 
-constexpr int kTrTile = 32;      // transpose tile (channels x pixels)
 constexpr int kNhPos = 128;      // output positions per block
 constexpr int kNhThreads = 256;
 constexpr int kNhChan = 64;      // channels per pass (8 lanes x 8 channels)
 constexpr int kNhLanes = 8;      // lanes per position
 constexpr size_t kNhChunkTarget = (size_t)512 << 20;   // workspace bytes asked for, at most
-
-// Element bits, moved unchanged by the transpose.
-template <typename T> using RawOf = typename std::conditional<sizeof(T) == 4, uint32_t, uint16_t>::type;
-
-// X[n, c, p] -> slot n of the workspace, pixel p, channel c; one 32 x 32
-// tile per block through shared memory, coalesced on both sides.  Block
-// (ct, pt, n) = blockIdx.x; blocks with pt = 0 also zero their channels of the
-// slot's zero pixel.  Elements move as raw bits.
-template <typename R>
-__global__ void __launch_bounds__(256)
-nchw_to_nhwc_kernel(const R *__restrict__ X, R *__restrict__ ws, int C, int64_t P, int ctiles,
-                    int64_t ptiles) {
-    __shared__ R tile[kTrTile][kTrTile + 1];
-    int64_t b = blockIdx.x;
-    const int ct = (int)(b % ctiles);
-    b /= ctiles;
-    const int64_t pt = b % ptiles;
-    const int64_t n = b / ptiles;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
-    const int c0 = ct * kTrTile;
-    const int64_t p0 = pt * kTrTile;
-    const R *src = X + n * C * P;
-    R *dst = ws + n * C * (P + 1) + C;   // pixel 0 of slot n
-    if (pt == 0 && ty == 0 && c0 + tx < C) dst[c0 + tx - C] = 0;
-#pragma unroll
-    for (int i = 0; i < kTrTile; i += 8) {
-        const int c = c0 + ty + i;
-        const int64_t p = p0 + tx;
-        if (c < C && p < P) tile[ty + i][tx] = src[(int64_t)c * P + p];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kTrTile; i += 8) {
-        const int64_t p = p0 + ty + i;
-        const int c = c0 + tx;
-        if (c < C && p < P) dst[p * C + c] = tile[tx][ty + i];
-    }
-}
 
 // One 16-byte vector of channels.
 template <typename T> struct Vec16 { static constexpr int E = 16 / (int)sizeof(T); };
@@ -305,9 +268,7 @@ static cudaError_t launch_nhwc_mode(const void *X, const void *grid, void *Y, co
     using R = RawOf<T>;
     const SampleArgs &a = P.a;
     const size_t slot = nhwc_slot_bytes(a, sizeof(T));
-    const int ctiles = (a.C + kTrTile - 1) / kTrTile;
-    const int64_t ptiles = (a.in_plane + kTrTile - 1) / kTrTile;
-    const int64_t tiles_img = ptiles * ctiles;   // copy tiles per image
+    const int64_t tiles_img = copy_tiles_per_image(a.C, a.in_plane);   // copy blocks per image
     // as many slots per chunk as the workspace holds (at least one), within
     // the 2^31 - 1 blocks of a launch
     const int64_t max_blocks = ((int64_t)1 << 31) - 1;
@@ -316,8 +277,8 @@ static cudaError_t launch_nhwc_mode(const void *X, const void *grid, void *Y, co
     per = std::min<int64_t>(per, std::max<int64_t>(1, max_blocks / a.tiles));
     for (int64_t n0 = 0; n0 < a.N; n0 += per) {
         const int64_t nc = std::min<int64_t>(per, a.N - n0);
-        nchw_to_nhwc_kernel<R><<<(unsigned)(nc * tiles_img), 256, 0, s>>>(
-            (const R *)X + n0 * a.C * a.in_plane, (R *)ws, a.C, a.in_plane, ctiles, ptiles);
+        launch_copy_to_slots<R>((const R *)X + n0 * a.C * a.in_plane, (R *)ws, nc, a.C,
+                                a.in_plane, s);
         nhwc_sample_kernel<T, MODE><<<(unsigned)(nc * a.tiles), kNhThreads, 0, s>>>(
             (const T *)ws, (const T *)grid, (T *)Y, P, (int)n0);
         const cudaError_t e = cudaGetLastError();

@@ -108,8 +108,11 @@ def test_affine_grid_checks(L):
 
 
 def _deform(L, x_shape=(1, 4, 8, 8), oC=4, kernel=(3, 3), pads=(1, 1, 1, 1), strides=(1, 1),
-            dil=(1, 1), group=1, og=1, X=FAKE):
+            dil=(1, 1), group=1, og=1, X=FAKE, ws=False):
     a = gs.deform_attrs(kernel, pads, strides, dil, group, og)
+    if ws:   # no workspace: checks as gs_deform_conv
+        return L.gs_deform_conv_ws(X, _i64(list(x_shape)), FAKE, oC, FAKE, None, None,
+                                   ctypes.byref(a), 0, None, 0, FAKE, None)
     return L.gs_deform_conv(X, _i64(list(x_shape)), FAKE, oC, FAKE, None, None, ctypes.byref(a), 0,
                             FAKE, None)
 
@@ -119,8 +122,25 @@ def _deform(L, x_shape=(1, 4, 8, 8), oC=4, kernel=(3, 3), pads=(1, 1, 1, 1), str
     (dict(strides=(0, 1)), 5), (dict(dil=(1, 0)), 5), (dict(pads=(-1, 0, 0, 0)), 5),
     (dict(x_shape=(1, 4, 2, 2), pads=(0, 0, 0, 0)), 3), (dict(X=None), 1),
 ])
-def test_deform_conv_rejects_bad_arguments(L, kwargs, status):
-    assert _deform(L, **kwargs) == status
+@pytest.mark.parametrize("ws", [False, True])
+def test_deform_conv_rejects_bad_arguments(L, kwargs, status, ws):
+    assert _deform(L, ws=ws, **kwargs) == status
+
+
+def test_deform_conv_workspace_size_queries(L):
+    n = ctypes.c_size_t(7)
+    a = gs.deform_attrs((3, 3), (1, 1, 1, 1))
+    # bf16, tensor-core shape: packed W (64*64*9*2 bytes) + 8 slots of (64*64 + 1) * 64 * 2
+    assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 2,
+                                           ctypes.byref(n)) == 0
+    assert n.value == 64 * 64 * 9 * 2 + 8 * (64 * 64 + 1) * 64 * 2
+    assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 0,
+                                           ctypes.byref(n)) == 0 and n.value == 0   # fp32
+    assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 2,
+                                           None) == 1
+    bad = gs.deform_attrs((3, 3), (1, 1, 1, 1), group=3)
+    assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(bad), 2,
+                                           ctypes.byref(n)) == 5
 
 
 def test_deform_conv_null_attrs(L):

@@ -123,3 +123,93 @@ def test_deform_conv_tensor_core_shapes(gs_cuda, oracle_mod, case, dtype):
     ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
                                    for n in ("X", "W", "offset", "B", "mask")], **kw)
     assert_parity(Y, ref, dtype, f"deform tc case {case} {dtype}")
+
+
+# ------------------------------------------------ channel-last workspace path
+
+@pytest.mark.parametrize("case,dtype", list(itertools.product(range(len(TC_CASES)),
+                                                              ["float16", "bfloat16"])))
+def test_deform_conv_workspace_matches(gs_cuda, oracle_mod, case, dtype):
+    """gs_deform_conv_ws: the same values as gs_deform_conv (same weights, same
+    order of accumulation), and the oracle's within the tolerance."""
+    N, C, H, W, oC, k, p, s, d, has_b, has_m = TC_CASES[case]
+    g = wl.rng(700 + case)
+    oH = (H + p[0] + p[2] - d[0] * (k[0] - 1) - 1) // s[0] + 1
+    oW = (W + p[1] + p[3] - d[1] * (k[1] - 1) - 1) // s[1] + 1
+    K = k[0] * k[1]
+    host = {
+        "X": wl.as_dtype(g.normal(size=(N, C, H, W)), dtype),
+        "W": wl.as_dtype(g.normal(0, 0.05, size=(oC, C) + k), dtype),
+        "offset": wl.as_dtype(g.normal(0, 2.0, size=(N, K * 2, oH, oW)), dtype),
+        "B": wl.as_dtype(g.normal(size=(oC,)), dtype) if has_b else None,
+        "mask": wl.as_dtype(g.uniform(0, 1, size=(N, K, oH, oW)), dtype) if has_m else None,
+    }
+    kw = dict(kernel_shape=k, pads=p, strides=s, dilations=d)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    args = (cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"])
+    assert gs_cuda.gs_deform_conv_workspace_size(
+        host["X"].shape, oC, gs_cuda.deform_attrs(k, p, s, d), getattr(torch, dtype)) > 0
+    Yw = gs_cuda.gs_deform_conv(*args, workspace="auto", **kw)
+    Y0 = gs_cuda.gs_deform_conv(*args, **kw)
+    assert gs_cuda.gs_device_status() == 0
+    assert torch.equal(Yw, Y0)
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Yw, ref, dtype, f"deform ws case {case} {dtype}")
+
+
+@pytest.mark.parametrize("slots", [1, 2])
+def test_deform_conv_workspace_chunks(gs_cuda, slots):
+    """A workspace with room for W and fewer image slots than N runs image chunks."""
+    g = wl.rng(720 + slots)
+    N, C, H, W, oC = 3, 32, 11, 13, 16
+    X = wl.as_dtype(g.normal(size=(N, C, H, W)), "bfloat16").cuda()
+    Wt = wl.as_dtype(g.normal(0, 0.05, size=(oC, C, 3, 3)), "bfloat16").cuda()
+    off = wl.as_dtype(g.normal(0, 1.5, size=(N, 18, H, W)), "bfloat16").cuda()
+    a = gs_cuda.deform_attrs((3, 3), (1, 1, 1, 1))
+    full = gs_cuda.gs_deform_conv_workspace_size(X.shape, oC, a, torch.bfloat16)
+    slot = C * (H * W + 1) * 2
+    ws = torch.empty(full - (N - slots) * slot, dtype=torch.uint8, device="cuda")
+    Yw = gs_cuda.gs_deform_conv(X, Wt, off, pads=(1, 1, 1, 1), workspace=ws)
+    assert torch.equal(Yw, gs_cuda.gs_deform_conv(X, Wt, off, pads=(1, 1, 1, 1)))
+
+
+def test_deform_conv_workspace_falls_back(gs_cuda):
+    """fp32, grouped shapes and a workspace short of W plus one slot run gs_deform_conv."""
+    g = wl.rng(730)
+    X = torch.from_numpy(g.normal(size=(2, 16, 9, 9)).astype(np.float32)).cuda()
+    Wt = torch.from_numpy(g.normal(0, 0.1, size=(16, 16, 3, 3)).astype(np.float32)).cuda()
+    off = torch.from_numpy(g.normal(0, 1, size=(2, 18, 9, 9)).astype(np.float32)).cuda()
+    a = gs_cuda.deform_attrs((3, 3), (1, 1, 1, 1))
+    assert gs_cuda.gs_deform_conv_workspace_size(X.shape, 16, a, torch.float32) == 0
+    assert torch.equal(gs_cuda.gs_deform_conv(X, Wt, off, pads=(1, 1, 1, 1), workspace="auto"),
+                       gs_cuda.gs_deform_conv(X, Wt, off, pads=(1, 1, 1, 1)))
+    Xh, Wh, oh = X.bfloat16(), Wt.bfloat16(), off.bfloat16()
+    small = torch.empty(16 * 16 * 9 * 2, dtype=torch.uint8, device="cuda")   # W only
+    assert torch.equal(gs_cuda.gs_deform_conv(Xh, Wh, oh, pads=(1, 1, 1, 1), workspace=small),
+                       gs_cuda.gs_deform_conv(Xh, Wh, oh, pads=(1, 1, 1, 1)))
+    Wg = Wh[:, :8].contiguous()                                             # group = 2
+    assert gs_cuda.gs_deform_conv_workspace_size(Xh.shape, 16, gs_cuda.deform_attrs(
+        (3, 3), (1, 1, 1, 1), group=2), torch.bfloat16) == 0
+    assert torch.equal(gs_cuda.gs_deform_conv(Xh, Wg, oh, pads=(1, 1, 1, 1), group=2,
+                                              workspace="auto"),
+                       gs_cuda.gs_deform_conv(Xh, Wg, oh, pads=(1, 1, 1, 1), group=2))
+
+
+def test_full_size_deform2d_workspace(gs_cuda, oracle_mod):
+    w = wl.WORKLOADS["deform2d"]
+    inp = wl.make_deform_inputs(w)
+    host = {k: wl.as_dtype(v, "bfloat16") for k, v in inp.items()}
+    cu = {k: v.cuda() for k, v in host.items()}
+    kw = dict(kernel_shape=w.kernel, pads=w.pads, strides=w.strides, dilations=w.dilations,
+              group=w.group, offset_group=w.offset_group)
+    args = (cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"])
+    Y = gs_cuda.gs_deform_conv(*args, workspace="auto", **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, gs_cuda.gs_deform_conv(*args, **kw))
+    g = wl.rng(6)
+    idx = np.unique(np.concatenate([g.integers(0, Y.numel(), 20000), [0, Y.numel() - 1]]))
+    ref = oracle_mod.deform_conv_at(exact(host["X"]), exact(host["W"]), exact(host["offset"]), idx,
+                                    exact(host["B"]), exact(host["mask"]), **kw)
+    assert_parity(Y.reshape(-1)[torch.from_numpy(idx).cuda()], ref, "bfloat16",
+                  "deform2d with workspace, sampled")

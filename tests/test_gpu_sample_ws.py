@@ -173,3 +173,21 @@ def test_full_size_gs2d_cubic_with_workspace(gs_cuda, oracle_mod, dtype, mode):
     # at any size: the same values as the NCHW gather
     assert torch.equal(Y, gs_cuda.gs_grid_sample(Xd, Gd, mode, w.padding_mode, w.align_corners,
                                                  w.cubic_coeff_a))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_workspace_unaligned_input(gs_cuda, oracle_mod, dtype):
+    """X one element past a 16-byte boundary: the copy reads it element by element."""
+    g = wl.rng(62)
+    xs, out = (2, 16, 12, 16), (9, 11)      # H*W a multiple of every vector width
+    Xt = wl.as_dtype(g.normal(size=xs), dtype)
+    Gt = wl.as_dtype(_grid(g, xs[0], out), dtype)
+    n = int(np.prod(xs))
+    buf = torch.empty(n + 8, dtype=Xt.dtype, device="cuda")
+    Xd = buf[1:n + 1].view(xs)
+    Xd.copy_(Xt.cuda())
+    assert Xd.data_ptr() % 16 != 0
+    Y = gs_cuda.gs_grid_sample_ws(Xd, Gt.cuda(), "auto", "linear", "reflection", 1)
+    ref = oracle_mod.grid_sample(exact(Xt), exact(Gt), "linear", "reflection", 1)
+    assert_parity(Y, ref, dtype, "unaligned X")
+    assert torch.equal(Y, gs_cuda.gs_grid_sample(Xd, Gt.cuda(), "linear", "reflection", 1))
