@@ -145,9 +145,14 @@ gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const 
  * gs_grid_sample_static -- gs_grid_sample_ws whose workspace is a fixed
  * GS_STATIC_WORKSPACE_BYTES array in the library's static device memory, so
  * the call allocates nothing (no cudaMalloc, no allocating library call) and
- * needs no caller buffer: for callers that may not allocate, such as code
- * being captured into a CUDA graph.  The operator pages have no counterpart
- * to this call; it is a deployment convenience around the same kernels.
+ * needs no caller buffer.  It is meant for callers that cannot allocate
+ * device memory at the point of the call: a plugin inside a host framework
+ * that owns all device memory through its own pool and hands out only
+ * inputs and outputs; a real-time loop that must not block, since
+ * cudaMalloc and cudaFree can synchronise the device; or code whose memory
+ * budget is fixed at start-up, where an allocation failing mid-run has no
+ * way to recover.  The operator pages have no counterpart to this call; it
+ * wraps the same kernels as gs_grid_sample_ws.
  *
  *   Arguments, results and errors as gs_grid_sample.  A call the channel-
  *   last path takes (see gs_grid_sample_workspace_size) whose image slot,

@@ -220,8 +220,11 @@ def gs_grid_sample_ws(X, grid, workspace="auto", mode="linear", padding_mode="ze
 
 def gs_grid_sample_static(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
                           cubic_coeff_a=-0.75, out=None):
-    """gs_grid_sample with the library's static scratch (see gs_grid_sample_static in
-    gs.h): no allocation in the call; concurrent calls race on the one scratch."""
+    """gs_grid_sample with its scratch in the library's static device memory
+    (gs_grid_sample_static in gs.h), for callers that cannot allocate device
+    memory at the call: the C entry point allocates nothing.  Pass ``out`` to keep
+    this wrapper from allocating the output with torch.  Concurrent calls race on
+    the one scratch; the first call on a device should precede any stream capture."""
     torch = _torch()
     _check_tensors(X, grid, out)
     r = X.dim() - 2

@@ -1,5 +1,9 @@
 """gs_grid_sample_static (scratch in the library's static device memory, no
-allocation in the call) against gs_grid_sample on the GPU.
+allocation in the call) against gs_grid_sample on the GPU.  The entry point
+exists for callers that cannot allocate device memory where they call it (a
+plugin whose host framework owns all device memory, a loop that must not block
+on cudaMalloc/cudaFree, a budget fixed at start-up); it shares one scratch
+array per device between all calls.
 
 Collected last on purpose: it must pass alone and after every other test, so
 nothing earlier may leave state it depends on.  Each case runs two calls in a
