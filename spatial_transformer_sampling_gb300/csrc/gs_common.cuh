@@ -33,12 +33,14 @@ template <> struct IO<float> {
     static __device__ __forceinline__ float ld(const float *p) { return __ldg(p); }
     static __device__ __forceinline__ float st(float v) { return v; }
     static __host__ __device__ __forceinline__ double to_double(float v) { return v; }
+    static __device__ __forceinline__ float to_f(float v) { return v; }
 };
 template <> struct IO<__half> {
     static __device__ __forceinline__ float ld(const __half *p) { return __half2float(__ldg(p)); }
     static __device__ __forceinline__ __half st(float v) { return __float2half_rn(v); }
     static __device__ __forceinline__ double to_double(__half v) { return __half2float(v); }
     static __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
 };
 template <> struct IO<__nv_bfloat16> {
     static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) {
@@ -49,6 +51,7 @@ template <> struct IO<__nv_bfloat16> {
         return __bfloat162float(v);
     }
     static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
 // ------------------------------------------------------------- axis params

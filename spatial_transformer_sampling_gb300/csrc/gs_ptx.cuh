@@ -86,6 +86,63 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2 only);
+// src_bytes < 16 zero-fills the rest, 0 writes sixteen zero bytes without
+// reading `src`.  Completion is tracked per thread in commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most `pending` (0, 1 or 2; more counts as 2) of this thread's
+// most recent commit groups are still in flight.
+__device__ __forceinline__ void cp_async_wait_pending(int pending) {
+    if (pending <= 0) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else if (pending == 1) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+    }
+}
+
+// Arrives once on `bar` when every cp.async this thread issued so far has
+// completed (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Plain arrive (release semantics: this thread's earlier shared-memory reads
+// and writes are ordered before it).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Packed fp32 pairs (Blackwell): lane-wise a*b and a*b+c, each rounded to
+// nearest exactly as fmulf / fmaf would round it.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
 }  // namespace gs
 
 // ------------------------------------------------------------------ tcgen05

@@ -2,7 +2,8 @@
 // standalone AffineGrid kernel (templates; instantiated once per dtype).
 //
 // sample_kernel (any rank, tensor grid or fused affine; gs_band.cuh streams
-// the fused 2-D case through shared memory instead): one thread per output
+// the fused 2-D case through shared memory instead, gs_vol.cuh the fused 3-D
+// trilinear and nearest cases): one thread per output
 // position, looping over all C channels.  Coordinates, padding and tap
 // weights are computed once per position in registers and reused by every
 // channel (GridSample - version 20: the grid vector is shared by all channels
@@ -327,6 +328,7 @@ inline Axis make_axis(int n, int ac) {
 
 #include "gs_band.cuh"
 #include "gs_nhwc.cuh"
+#include "gs_vol.cuh"
 
 namespace gs {
 
@@ -336,6 +338,11 @@ static cudaError_t launch_sample_t(const void *X, const void *src, void *Y, Samp
     if constexpr (AFFINE && R == 2) {
         bool used = false;
         const cudaError_t e = launch_band<T, MODE>(X, src, Y, P, s, &used);
+        if (used || e != cudaSuccess) return e;
+    }
+    if constexpr (AFFINE && R == 3 && MODE != MODE_CUBIC) {
+        bool used = false;
+        const cudaError_t e = launch_vol<T, MODE>(X, src, Y, P, s, &used);
         if (used || e != cudaSuccess) return e;
     }
 
