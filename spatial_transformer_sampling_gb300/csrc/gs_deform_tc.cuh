@@ -344,8 +344,15 @@ deform_tc_nhwc_kernel(const T *__restrict__ Xs, const uint4 *__restrict__ wpk,
     const int C = a.C, oC = a.oC, K = a.kH * a.kW;
     const int chunks_per_tap = C / KC;
     const int nchunks = K * chunks_per_tap;
+    // 64-channel chunks use the 128-byte-swizzled A layout: the eight lanes that
+    // store one position's eight channel octets then hit eight different bank
+    // groups (unswizzled, the octets sit 128 bytes apart and collide).
+    constexpr bool kSwz = KC == 64;
     unsigned char *w_s = tc_smem;                      // packed W
-    unsigned char *a_s = tc_smem + q.w_bytes;          // two A buffers
+    // two A buffers, 1024-byte aligned (the swizzle atom); the launch asks for
+    // 1 KB of slack
+    const uint32_t a_pad = (1024u - ((smem_u32(tc_smem) + q.w_bytes) & 1023u)) & 1023u;
+    unsigned char *a_s = tc_smem + q.w_bytes + a_pad;
     constexpr uint32_t a_buf_bytes = (uint32_t)kTcM * KC * 2;
     constexpr uint32_t sbo_a = (uint32_t)KC * 16;      // 8 rows x KC channels x 2 bytes
     const uint32_t sbo_b = (uint32_t)C * 16;
@@ -453,7 +460,10 @@ deform_tc_nhwc_kernel(const T *__restrict__ Xs, const uint4 *__restrict__ wpk,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = fmaf(w, IO<T>::to_float(h[e]), v[e]);
             }
-            *reinterpret_cast<uint4 *>(abuf + (pl / 8) * sbo_a + j * 128 + (pl % 8) * 16) =
+            const uint32_t a_off = kSwz ? (uint32_t)((pl / 8) * 1024 + (pl % 8) * 128 +
+                                                     ((j ^ (pl % 8)) << 4))
+                                        : (uint32_t)((pl / 8) * sbo_a + j * 128 + (pl % 8) * 16);
+            *reinterpret_cast<uint4 *>(abuf + a_off) =
                 make_uint4(pack_pair<T>(v[0], v[1]), pack_pair<T>(v[2], v[3]),
                            pack_pair<T>(v[4], v[5]), pack_pair<T>(v[6], v[7]));
         }
@@ -472,7 +482,8 @@ deform_tc_nhwc_kernel(const T *__restrict__ Xs, const uint4 *__restrict__ wpk,
                     smem_u32(w_s) + (uint32_t)k * slice_b + (uint32_t)(cb * KC / 8) * 128;
 #pragma unroll
                 for (int ks = 0; ks < KC / 16; ++ks) {
-                    const uint64_t ad = umma_desc_kmajor(a_addr + ks * 256, 128, sbo_a);
+                    const uint64_t ad = kSwz ? umma_desc_kmajor_sw128(a_addr + ks * 32, 1024)
+                                             : umma_desc_kmajor(a_addr + ks * 256, 128, sbo_a);
                     const uint64_t bd = umma_desc_kmajor(b_addr + ks * 256, 128, sbo_b);
                     umma_f16(tmem_d, ad, bd, idesc, (chunk > 0 || ks > 0) ? 1u : 0u);
                 }
@@ -542,7 +553,7 @@ inline bool deform_tc_params(const DeformArgs &a, DeformTcParams *q, size_t *sme
     const int P = a.oH * a.oW;
     q->tiles = (P + kTcM - 1) / kTcM;
     q->w_bytes = (uint32_t)a.kH * a.kW * a.oC * a.C * 2;
-    *smem = (size_t)q->w_bytes + 2 * (size_t)kTcM * q->kc * 2;
+    *smem = (size_t)q->w_bytes + 2 * (size_t)kTcM * q->kc * 2 + 1024;   // + alignment slack
     if (*smem > (size_t)kTcMaxSmem) return false;
     uint32_t cols = 32;
     while (cols < (uint32_t)a.oC) cols <<= 1;

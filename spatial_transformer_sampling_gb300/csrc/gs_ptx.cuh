@@ -170,6 +170,22 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t smem_addr, uint32_
     return d;
 }
 
+// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:
+// each row (M or N index) holds 64 two-byte K elements in 128 bytes, 8 rows
+// form a 1024-byte atom, and the 16-byte chunk c of row r is stored at chunk
+// c ^ (r % 8) of that row (the atom must be 1024-byte aligned).  `sbo` is the
+// byte distance between 8-row atoms; a K step of 16 elements inside the atom
+// moves the start address by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t smem_addr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1 << 16;                               // leading offset: unused with this swizzle
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;          // stride-dimension byte offset
+    d |= (uint64_t)1 << 46;                               // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                               // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for kind::f16: fp32 accumulator, A and B both bf16
 // (is_bf16) or both fp16, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(bool is_bf16, int M, int N) {
