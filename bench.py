@@ -309,7 +309,7 @@ def time_e2e(case, steps, warmup):
     out_host = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = out_host.numel() * out_host.element_size()
-    streamer = gs.HostStreamer(case.device, chunks=8)
+    streamer = gs.HostStreamer(case.device)
 
     if w.kind == "affine_sample":
         def step():

@@ -345,10 +345,15 @@ class HostStreamer:
     in the result.  Device buffers are allocated once per shape and reused.
     """
 
-    def __init__(self, device=None, chunks=8):
+    # With chunks=None the batch is cut into chunks of about this many input
+    # bytes (whole images): the first chunk's upload and the last chunk's
+    # download are not overlapped with anything, so smaller chunks cost less.
+    CHUNK_BYTES = 4 << 20
+
+    def __init__(self, device=None, chunks=None):
         torch = _torch()
         self.device = torch.device(device or "cuda")
-        self.chunks = int(chunks)
+        self.chunks = None if chunks is None else int(chunks)
         self.s_in = torch.cuda.Stream(self.device)
         self.s_run = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
@@ -365,7 +370,12 @@ class HostStreamer:
         (batch_axes[i] is None for inputs passed whole); out_host is filled in place."""
         torch = _torch()
         N = out_host.shape[0]
-        step = max(1, -(-N // self.chunks))
+        chunks = self.chunks
+        if chunks is None:
+            in_bytes = sum(t.numel() * t.element_size() for t, ax in zip(inputs, batch_axes)
+                           if ax is not None)
+            chunks = max(1, min(N, in_bytes // self.CHUNK_BYTES))
+        step = max(1, -(-N // chunks))
         key = (tuple((tuple(t.shape), t.dtype) for t in inputs), tuple(out_host.shape),
                out_host.dtype)
         dev = self._buffers(key, [t.shape for t in inputs] + [out_host.shape], out_host.dtype)
@@ -409,7 +419,7 @@ def gs_affine_sample_from_host(theta, size, X, mode="linear", padding_mode="zero
     size = [int(s) for s in size]
     if out is None:
         out = torch.empty(list(X.shape[:2]) + size[2:], dtype=X.dtype).pin_memory()
-    st = streamer or HostStreamer(chunks=8)
+    st = streamer or HostStreamer()
 
     def fn(th, x, out):
         n = x.shape[0]
@@ -427,7 +437,7 @@ def gs_grid_sample_from_host(X, grid, mode="linear", padding_mode="zeros", align
     torch = _torch()
     if out is None:
         out = torch.empty(list(X.shape[:2]) + list(grid.shape[1:-1]), dtype=X.dtype).pin_memory()
-    st = streamer or HostStreamer(chunks=8)
+    st = streamer or HostStreamer()
 
     def fn(x, g, out):
         ws = workspace

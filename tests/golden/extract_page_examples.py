@@ -43,17 +43,9 @@ DEFORM_NAMES = ["test_cc_basic_deform_conv_with_padding",
                 "test_cc_basic_deform_conv_without_padding",
                 "test_cc_deform_conv_with_mask_bias",
                 "test_cc_deform_conv_with_multiple_offset_groups"]
-# Resize examples whose sampling is plain separable interpolation (no antialias);
-# the exclude_outside ones are kept too, the test uses only their interior points.
-RESIZE_NAMES = [
-    "_resize_upsample_scales_cubic", "_resize_upsample_scales_cubic_align_corners",
-    "_resize_upsample_scales_cubic_asymmetric", "_resize_downsample_scales_cubic",
-    "_resize_downsample_scales_cubic_align_corners", "_resize_upsample_sizes_cubic",
-    "_resize_downsample_sizes_cubic", "_resize_upsample_scales_cubic_A_n0p5_exclude_outside",
-    "_resize_downsample_scales_cubic_A_n0p5_exclude_outside",
-    "_resize_upsample_scales_linear", "_resize_upsample_scales_linear_align_corners",
-    "_resize_downsample_scales_linear", "_resize_downsample_scales_linear_align_corners",
-]
+# Resize: every example on the page (found by name in main()); the ones
+# listed here were the first transcribed and keep their fixture names.
+RESIZE_MARKER = re.compile(r"\*\*(_resize_[A-Za-z0-9_]+)\*\*")
 
 NUM = re.compile(r"-?\d+\.\d*(?:[eE][-+]?\d+)?|-?\d+(?:[eE][-+]?\d+)?|-?\.\d+")
 
@@ -174,32 +166,60 @@ def onnx_fixture(op, page, name, seg):
             "notes": notes}
 
 
+def _resize_value(v, env):
+    """A make_node keyword value: a literal, or a variable assigned earlier in the example."""
+    if v.startswith('"'):
+        return v.strip('"')
+    if v in ("True", "False"):
+        return int(v == "True")
+    if re.fullmatch(r"-?[\d.]+", v):
+        return float(v) if "." in v else int(v)
+    return env[v]
+
+
 def resize_fixture(name, seg):
+    # variables the example assigns before make_node (axes, keep_aspect_ratio_policy)
+    env = {}
+    head = seg[:seg.index("make_node(")]
+    for k, v in re.findall(r"(\w+)\s*=\s*(\"[^\"]*\"|\[[^\]]*\])", head):
+        env[k] = v.strip('"') if v.startswith('"') else [int(x) for x in NUM.findall(v)]
     attrs = {}
     node = re.search(r"make_node\((.*?)\)\s*data", seg, re.S).group(1)
-    for k, v in re.findall(r"(\w+)=(\"[^\"]*\"|-?[\d.]+|True|False)", node):
-        if v.startswith('"'):
-            attrs[k] = v.strip('"')
-        elif v in ("True", "False"):
-            attrs[k] = int(v == "True")
-        else:
-            attrs[k] = float(v) if "." in v else int(v)
+    for k, v in re.findall(r"(\w+)=(\"[^\"]*\"|-?[\d.]+|True|False|[A-Za-z_]\w*)", node):
+        if k in ("inputs", "outputs"):
+            continue
+        attrs[k] = _resize_value(v, env)
     data_txt, _ = balanced(seg, seg.index("data = np.array("))
     data = np.array(nested(data_txt), dtype=np.float64)
     ins = {"X": tensor_entry(data.shape, "float32", data.ravel())}
+    m = re.search(r"\broi = np\.array\(", seg)
+    if m:
+        roi_txt, _ = balanced(seg, m.end() - 1)
+        roi = [float(v) for v in NUM.findall(roi_txt)]
+        ins["roi"] = tensor_entry([len(roi)], "float32", roi)
     m = re.search(r"(scales|sizes) = np\.array\(", seg)
-    vec_txt, _ = balanced(seg, m.end() - 1)
+    vec_txt, vec_end = balanced(seg, m.end() - 1)
     vec = [float(v) for v in NUM.findall(vec_txt)]
     if m.group(1) == "scales":
         ins["scales"] = tensor_entry([len(vec)], "float32", vec)
     else:
         ins["sizes"] = tensor_entry([len(vec)], "int64", vec)
-    exp_txt, _ = balanced(seg, seg.index("# [") + 2)
+    exp_txt, _ = balanced(seg, seg.index("# [", vec_end) + 2)
     exp = np.array(nested(exp_txt), dtype=np.float64)
-    return {"citation": f"{RESIZE}, Examples, {name}", "op": "Resize", "name": name,
-            "attributes": attrs, "inputs": ins,
-            "outputs": {"Y": tensor_entry(exp.shape, "float32", exp.ravel())},
-            "notes": ["expected output is the array printed in the example's comment"]}
+    fx = {"citation": f"{RESIZE}, Examples, {name}", "op": "Resize", "name": name,
+          "attributes": attrs, "inputs": ins,
+          "outputs": {"Y": tensor_entry(exp.shape, "float32", exp.ravel())},
+          "notes": ["expected output is the array printed in the example's comment"]}
+    # some examples state the output extent in words ("# Results in 8x8")
+    m = re.search(r"# Results in (\d+)x(\d+)", seg[vec_end:])
+    if m:
+        stated = [int(m.group(1)), int(m.group(2))]
+        fx["stated_spatial_shape"] = stated
+        if list(exp.shape[-2:]) != stated:
+            fx["notes"].append(f"the page states {stated[0]}x{stated[1]} but prints "
+                               f"{exp.shape[-2]}x{exp.shape[-1]}: the printed rows are read as "
+                               "the first rows of the stated output")
+    return fx
 
 
 def main():
@@ -214,7 +234,8 @@ def main():
         fixtures.append(onnx_fixture("GridSample", GRIDSAMPLE, n, seg))
     for n, seg in segments(text, DEFORM_NAMES, lambda n: rf"\*\*{re.escape(n)}\*\*").items():
         fixtures.append(onnx_fixture("DeformConv", DEFORM, n, seg))
-    for n, seg in segments(text, RESIZE_NAMES, lambda n: rf"\*\*{re.escape(n)}\*\*").items():
+    resize_names = list(dict.fromkeys(RESIZE_MARKER.findall(text)))
+    for n, seg in segments(text, resize_names, lambda n: rf"\*\*{re.escape(n)}\*\*").items():
         fixtures.append(resize_fixture(n, seg))
     for fx in fixtures:
         path = os.path.join(out_dir, f"{fx['op'].lower()}__{fx['name'].lstrip('_')}.json")

@@ -68,7 +68,7 @@ def _run_pins():
         attempt(n, pages.test_grid_sample_page_example, n)
     for n in fixture_names("deformconv__"):
         attempt(n, pages.test_deform_conv_page_example, n)
-    for n in fixture_names("resize__"):
+    for n in pages.resize_via_grid_sample_names():
         attempt(n, pages.test_resize_examples_through_grid_sample, n)
     for case in [(2, m, p, ac) for m in ("linear", "nearest", "cubic")
                  for p in ("zeros", "border", "reflection") for ac in (0, 1)]:
