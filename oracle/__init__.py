@@ -108,10 +108,16 @@ def _bind(L):
                                     ctypes.POINTER(_DeformAttrs), _i64p, ctypes.c_int64, _f64p]
     L.or_deform_out_extent.argtypes = [ctypes.c_int64] * 6
     L.or_deform_out_extent.restype = ctypes.c_int64
+    L.or_resize_shape.argtypes = [ctypes.c_int, _i64p, _i64p, ctypes.c_int, _f64p, _i64p, _f64p,
+                                  ctypes.c_int, ctypes.c_int, _i64p, _f64p, _f64p, _f64p, _f64p]
+    L.or_resize.argtypes = [_f64p, ctypes.c_int, _i64p, _i64p, _f64p, _f64p, _f64p, _f64p,
+                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                            ctypes.c_int, ctypes.c_double, ctypes.c_int, _f64p]
     L.or_set_num_threads.argtypes = [ctypes.c_int]
     L.or_max_threads.restype = ctypes.c_int
     for f in ("or_affine_grid", "or_grid_sample", "or_grid_sample_at", "or_affine_sample",
-              "or_affine_sample_at", "or_deform_conv", "or_deform_conv_at"):
+              "or_affine_sample_at", "or_deform_conv", "or_deform_conv_at", "or_resize_shape",
+              "or_resize"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -256,3 +262,52 @@ def deform_conv_at(X, W, offset, flat_idx, B=None, mask=None, kernel_shape=None,
                                    _p(mask), ctypes.byref(at), _p(idx, _i64p), idx.size,
                                    _p(vals)))
     return vals
+
+
+RESIZE_MODES = {"nearest": 1, "linear": 0, "cubic": 2}
+RESIZE_COORDS = {"half_pixel": 0, "pytorch_half_pixel": 1, "align_corners": 2, "asymmetric": 3,
+                 "tf_crop_and_resize": 4}
+RESIZE_NEAREST = {"round_prefer_floor": 0, "round_prefer_ceil": 1, "floor": 2, "ceil": 3}
+RESIZE_KEEP = {"stretch": 0, "not_larger": 1, "not_smaller": 2}
+
+
+def resize_shape(x_shape, scales=None, sizes=None, roi=None, axes=None,
+                 coordinate_transformation_mode="half_pixel", keep_aspect_ratio_policy="stretch"):
+    """Resize output extents and per-axis (scale, length_resized, roi_start, roi_end)."""
+    xs = _i64(x_shape)
+    rank = xs.size
+    ax = _i64(axes) if axes is not None else None
+    na = 0 if ax is None else ax.size
+    sc = _f64(scales) if scales is not None else None
+    sz = _i64(sizes) if sizes is not None else None
+    ro = _f64(roi) if roi is not None else None
+    out = np.empty(rank, dtype=np.int64)
+    scale, lres, r0, r1 = (np.empty(rank, dtype=np.float64) for _ in range(4))
+    _check(lib().or_resize_shape(rank, _p(xs, _i64p), _p(ax, _i64p), na, _p(sc), _p(sz, _i64p),
+                                 _p(ro), RESIZE_COORDS[coordinate_transformation_mode],
+                                 RESIZE_KEEP[keep_aspect_ratio_policy], _p(out, _i64p),
+                                 _p(scale), _p(lres), _p(r0), _p(r1)))
+    return tuple(int(v) for v in out), scale, lres, r0, r1
+
+
+def resize(X, scales=None, sizes=None, roi=None, axes=None, mode="nearest",
+           coordinate_transformation_mode="half_pixel", nearest_mode="round_prefer_floor",
+           cubic_coeff_a=-0.75, exclude_outside=0, extrapolation_value=0.0, antialias=0,
+           keep_aspect_ratio_policy="stretch"):
+    """Resize - 18 on an N-D array (one of scales / sizes, for `axes` or all axes)."""
+    X = _f64(X)
+    out, scale, lres, r0, r1 = resize_shape(X.shape, scales, sizes, roi, axes,
+                                            coordinate_transformation_mode,
+                                            keep_aspect_ratio_policy)
+    Y = np.empty(out, dtype=np.float64)
+    if Y.size == 0:
+        return Y
+    xs = _i64(X.shape)
+    os_ = _i64(out)
+    _check(lib().or_resize(_p(X), X.ndim, _p(xs, _i64p), _p(os_, _i64p), _p(scale), _p(lres),
+                           _p(r0), _p(r1), RESIZE_MODES[mode],
+                           RESIZE_COORDS[coordinate_transformation_mode],
+                           RESIZE_NEAREST[nearest_mode], float(cubic_coeff_a),
+                           int(exclude_outside), float(extrapolation_value), int(antialias),
+                           _p(Y)))
+    return Y

@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain double-precision CPU definition of the spatial-transformer
- * sampling path: AffineGrid, GridSample, the two fused, and DeformConv.
+ * sampling path: AffineGrid, GridSample, the two fused, DeformConv, and
+ * Resize.
  *
  * TEST INFRASTRUCTURE ONLY.  This is the independent checker for the CUDA
  * library.  Only the tests, the smoke check and the bench's CPU-baseline leg
@@ -21,7 +22,8 @@
  *   [DC]  DeformConv (ai.onnx, since version 22): Inputs (X, W, offset, B,
  *         mask) and Examples (kernel_shape, pads, offset_group).
  *   [RS]  Resize - 18: attribute cubic_coeff_a (names the cubic convolution
- *         kernel of Keys, "Equation (4)", with coefficient a).
+ *         kernel of Keys, "Equation (4)", with coefficient a); Summary,
+ *         Attributes and Inputs for the Resize operator itself.
  */
 #include <math.h>
 #include <stdint.h>
@@ -449,4 +451,239 @@ int or_deform_conv_at(const double *X, const int64_t *x_shape, const double *Wt,
     for (int64_t i = 0; i < count; ++i)
         out[i] = deform_elem(X, x_shape, Wt, oC, offset, B, mask, at, flat_idx[i]);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Resize                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* [RS] Resize - 18 (Summary, Attributes, Inputs).  Every axis is mapped on its
+ * own; the output value is the sum, over the tensor product of the per-axis
+ * taps, of the product of the 1-D weights times X at the tap.  Readings (the
+ * helper functions the page's examples call are not printed, so these are
+ * taken from the attribute text and checked against the printed outputs):
+ *  - a tap index outside [0, n-1] reads the edge value (index clamped), except
+ *    that exclude_outside=1 gives such taps weight 0 and rescales the rest to
+ *    sum 1;
+ *  - linear: taps floor(x), floor(x)+1, weights 1-t, t;  cubic: taps
+ *    floor(x)-1 .. floor(x)+2, Keys weights at distances t+1, t, 1-t, 2-t;
+ *  - antialias with scale < 1 stretches the filter by 1/scale: the taps are
+ *    the integer offsets k from floor(x) where the stretched filter can be
+ *    nonzero (linear: k = s .. 1-s with s = floor(-1/scale)+1; cubic:
+ *    k = s .. 1-s with s = floor(-2/scale)+1), weight filter((k-t)*scale),
+ *    rescaled to sum 1;
+ *  - with "scales" given the coordinate maps use that scale, and
+ *    length_resized = n_in * scale, unfloored; with "sizes" given,
+ *    scale = length_resized / length_original with length_resized the size;
+ *  - tf_crop_and_resize: a coordinate outside [0, n-1] on any axis makes the
+ *    whole output element extrapolation_value. */
+enum { RS_HALF_PIXEL = 0, RS_PYTORCH_HALF_PIXEL = 1, RS_ALIGN_CORNERS = 2, RS_ASYMMETRIC = 3,
+       RS_TF_CROP_AND_RESIZE = 4 };
+enum { RS_ROUND_PREFER_FLOOR = 0, RS_ROUND_PREFER_CEIL = 1, RS_FLOOR = 2, RS_CEIL = 3 };
+enum { RS_STRETCH = 0, RS_NOT_LARGER = 1, RS_NOT_SMALLER = 2 };
+#define RS_MAX_TAPS 4096
+
+/* [RS] coordinate_transformation_mode: x_original of output index x_resized. */
+static double rs_source_coord(double xr, int64_t n_in, int64_t n_out, double scale,
+                              double length_resized, double start, double end, int coord) {
+    switch (coord) {
+        case RS_PYTORCH_HALF_PIXEL:
+            return n_out > 1 ? (xr + 0.5) / scale - 0.5 : 0.0;
+        case RS_ALIGN_CORNERS:
+            /* a single output position has no second corner: it sits at 0 */
+            return length_resized > 1.0 ? xr * (double)(n_in - 1) / (length_resized - 1.0) : 0.0;
+        case RS_ASYMMETRIC:
+            return xr / scale;
+        case RS_TF_CROP_AND_RESIZE:
+            if (n_out > 1)
+                return start * (double)(n_in - 1) +
+                       xr * (end - start) * (double)(n_in - 1) / (double)(n_out - 1);
+            return 0.5 * (start + end) * (double)(n_in - 1);
+        default: /* half_pixel */
+            return (xr + 0.5) / scale - 0.5;
+    }
+}
+
+/* [RS] nearest_mode: the nearest pixel of x_original. */
+static double rs_nearest(double x, int nearest_mode) {
+    switch (nearest_mode) {
+        case RS_ROUND_PREFER_CEIL: return floor(x + 0.5);   /* halfway rounds up */
+        case RS_FLOOR: return floor(x);
+        case RS_CEIL: return ceil(x);
+        default: return ceil(x - 0.5);                     /* halfway rounds down */
+    }
+}
+
+/* Taps of one axis for output index o; returns the tap count, or -1 when the
+ * element takes extrapolation_value (tf_crop_and_resize outside the input). */
+static int rs_axis_taps(int64_t o, int64_t n_in, int64_t n_out, double scale,
+                        double length_resized, double start, double end, int coord, int mode,
+                        int nearest_mode, double a, int exclude_outside, int antialias,
+                        int64_t *idx, double *w) {
+    const double x = rs_source_coord((double)o, n_in, n_out, scale, length_resized, start, end,
+                                     coord);
+    if (coord == RS_TF_CROP_AND_RESIZE && (x < 0.0 || x > (double)(n_in - 1))) return -1;
+    int cnt;
+    if (mode == OR_NEAREST) {
+        idx[0] = to_index(rs_nearest(x, nearest_mode));
+        w[0] = 1.0;
+        cnt = 1;
+    } else {
+        const double f = floor(x), t = x - f;
+        const int64_t i0 = to_index(f);
+        const double s = (antialias && scale < 1.0) ? scale : 1.0;
+        /* first offset from floor(x) at which the (stretched) filter can be nonzero */
+        const double reach = mode == OR_LINEAR ? 1.0 : 2.0;
+        const int64_t k0 = (int64_t)floor(-reach / s) + 1;
+        const int64_t k1 = 1 - k0;   /* last offset, the mirror image of k0 */
+        if (k1 - k0 + 1 > RS_MAX_TAPS) return -2;
+        cnt = 0;
+        double sum = 0.0;
+        for (int64_t k = k0; k <= k1; ++k) {
+            const double d = ((double)k - t) * s;
+            const double wk = mode == OR_LINEAR ? fmax(0.0, 1.0 - fabs(d)) : keys(d, a);
+            idx[cnt] = i0 + k;
+            w[cnt] = wk;
+            sum += wk;
+            ++cnt;
+        }
+        if (s < 1.0) {
+            for (int k = 0; k < cnt; ++k) w[k] /= sum;
+        }
+    }
+    if (exclude_outside) {
+        double sum = 0.0;
+        for (int k = 0; k < cnt; ++k) {
+            if (idx[k] < 0 || idx[k] > n_in - 1) w[k] = 0.0;
+            sum += w[k];
+        }
+        if (sum != 0.0)
+            for (int k = 0; k < cnt; ++k) w[k] /= sum;
+    }
+    for (int k = 0; k < cnt; ++k) idx[k] = idx[k] < 0 ? 0 : (idx[k] > n_in - 1 ? n_in - 1 : idx[k]);
+    return cnt;
+}
+
+/* [RS] output extents and per-axis coordinate parameters from scales or sizes
+ * (one of them, for the axes listed in `axes`, or for all axes when naxes is
+ * 0).  keep_aspect_ratio_policy applies to sizes: not_larger / not_smaller
+ * take one common scale, the smallest / largest of sizes[i] / in[axes[i]],
+ * and round scale * in to the nearest integer, halfway up.  Writes out_shape,
+ * scale and length_resized per axis (rank entries); returns 0, or -1 on a bad
+ * argument. */
+int or_resize_shape(int rank, const int64_t *in_shape, const int64_t *axes, int naxes,
+                    const double *scales, const int64_t *sizes, const double *roi, int coord,
+                    int keep_policy, int64_t *out_shape, double *scale, double *length_resized,
+                    double *roi_start, double *roi_end) {
+    if (rank < 1 || rank > OR_MAX_RANK || (!scales && !sizes) || (scales && sizes)) return -1;
+    int ax[OR_MAX_RANK];
+    const int na = naxes > 0 ? naxes : rank;
+    for (int i = 0; i < na; ++i) {
+        int d = naxes > 0 ? (int)axes[i] : i;
+        if (d < 0) d += rank;
+        if (d < 0 || d >= rank) return -1;
+        ax[i] = d;
+    }
+    for (int d = 0; d < rank; ++d) {
+        out_shape[d] = in_shape[d];
+        scale[d] = 1.0;
+        length_resized[d] = (double)in_shape[d];
+        roi_start[d] = 0.0;
+        roi_end[d] = 1.0;
+    }
+    if (roi && coord == RS_TF_CROP_AND_RESIZE) {
+        for (int i = 0; i < na; ++i) {
+            roi_start[ax[i]] = roi[i];
+            roi_end[ax[i]] = roi[na + i];
+        }
+    }
+    if (scales) {
+        for (int i = 0; i < na; ++i) {
+            const int d = ax[i];
+            if (!(scales[i] > 0.0)) return -1;
+            const double len = (double)in_shape[d] * (roi_end[d] - roi_start[d]) * scales[i];
+            out_shape[d] = (int64_t)floor(len);
+            scale[d] = scales[i];
+            length_resized[d] = len;
+        }
+        return 0;
+    }
+    double common = 0.0;
+    if (keep_policy != RS_STRETCH) {
+        for (int i = 0; i < na; ++i) {
+            const double r = (double)sizes[i] / (double)in_shape[ax[i]];
+            if (i == 0 || (keep_policy == RS_NOT_LARGER ? r < common : r > common)) common = r;
+        }
+    }
+    for (int i = 0; i < na; ++i) {
+        const int d = ax[i];
+        const int64_t o = keep_policy == RS_STRETCH
+                              ? sizes[i]
+                              : (int64_t)floor(common * (double)in_shape[d] + 0.5);
+        if (o < 0) return -1;
+        out_shape[d] = o;
+        scale[d] = in_shape[d] > 0 ? (double)o / (double)in_shape[d] : 1.0;
+        length_resized[d] = (double)o;
+    }
+    return 0;
+}
+
+/* [RS] Y = Resize(X): direct summation over the tensor product of the taps. */
+int or_resize(const double *X, int rank, const int64_t *in_shape, const int64_t *out_shape,
+              const double *scale, const double *length_resized, const double *roi_start,
+              const double *roi_end, int mode, int coord, int nearest_mode, double a,
+              int exclude_outside, double extrapolation_value, int antialias, double *Y) {
+    if (rank < 1 || rank > OR_MAX_RANK) return -1;
+    const int64_t total = prod(out_shape, rank);
+    int bad = 0;
+#pragma omp parallel reduction(| : bad)
+    {
+        /* per-thread tap buffers */
+        int64_t *idx_buf = (int64_t *)malloc(sizeof(int64_t) * RS_MAX_TAPS * OR_MAX_RANK);
+        double *w_buf = (double *)malloc(sizeof(double) * RS_MAX_TAPS * OR_MAX_RANK);
+        if (!idx_buf || !w_buf) bad = 1;
+#pragma omp for schedule(dynamic, 64)
+        for (int64_t e = 0; e < total; ++e) {
+            if (!idx_buf || !w_buf) continue;
+            int64_t o[OR_MAX_RANK];
+            int64_t rem = e;
+            for (int d = rank - 1; d >= 0; --d) {
+                o[d] = rem % out_shape[d];
+                rem /= out_shape[d];
+            }
+            int cnt[OR_MAX_RANK];
+            int extrap = 0, err = 0;
+            for (int d = 0; d < rank && !extrap && !err; ++d) {
+                cnt[d] = rs_axis_taps(o[d], in_shape[d], out_shape[d], scale[d], length_resized[d],
+                                      roi_start[d], roi_end[d], coord, mode, nearest_mode, a,
+                                      exclude_outside, antialias, idx_buf + d * RS_MAX_TAPS,
+                                      w_buf + d * RS_MAX_TAPS);
+                if (cnt[d] == -1) extrap = 1;
+                if (cnt[d] < -1) err = 1;
+            }
+            double acc = 0.0;
+            if (extrap) {
+                acc = extrapolation_value;
+            } else if (!err) {
+                int k[OR_MAX_RANK] = {0};
+                for (;;) {
+                    double wt = 1.0;
+                    int64_t off = 0;
+                    for (int d = 0; d < rank; ++d) {
+                        wt *= w_buf[d * RS_MAX_TAPS + k[d]];
+                        off = off * in_shape[d] + idx_buf[d * RS_MAX_TAPS + k[d]];
+                    }
+                    acc += wt * X[off];
+                    int d = rank - 1;
+                    while (d >= 0 && ++k[d] == cnt[d]) k[d--] = 0;
+                    if (d < 0) break;
+                }
+            }
+            bad |= err;
+            Y[e] = acc;
+        }
+        free(idx_buf);
+        free(w_buf);
+    }
+    return bad ? -1 : 0;
 }

@@ -3,8 +3,8 @@
 Every mutation edits one spot of oracle.c (a dropped term, a wrong sign or
 index, a swapped operand), is compiled on the CPU into a temporary library,
 and must make at least one of the pin checks fail: the pages' worked
-examples, the Resize pins, the dense brute force, the torch cross-checks or
-the DeformConv special cases.  A mutation that no pin notices would mean the
+examples, the Resize pins, the dense brute force, the torch cross-checks,
+the DeformConv special cases or the Resize operator's own pins.  A mutation that no pin notices would mean the
 oracle could carry that mistake silently.  All mutations keep memory access
 in bounds.
 """
@@ -15,6 +15,7 @@ import pytest
 import oracle
 import test_oracle_pages as pages
 import test_oracle_pins as pins
+import test_oracle_resize as resize_pins
 from conftest import fixture_names
 
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
@@ -49,6 +50,33 @@ MUTATIONS = {
                         "(double)(ow * at->strides[1] + at->pads[1]"),
     "deform_group_offset_ignored": ("int64_t c = g * Cg + ci;", "int64_t c = ci;"),
     "deform_dilation_dropped": ("+ kw * at->dilations[1]) + dx", "+ kw) + dx"),
+    "resize_nearest_prefer_floor_rounds_up": ("default: return ceil(x - 0.5);",
+                                              "default: return floor(x + 0.5);"),
+    "resize_half_pixel_no_shift": ("default: /* half_pixel */\n            return (xr + 0.5) / scale - 0.5;",
+                                   "default: /* half_pixel */\n            return xr / scale;"),
+    "resize_align_corners_floored_length": (
+        "xr * (double)(n_in - 1) / (length_resized - 1.0)",
+        "xr * (double)(n_in - 1) / ((double)n_out - 1.0)"),
+    "resize_antialias_unnormalised": ("if (s < 1.0) {\n            for (int k = 0; k < cnt; ++k) w[k] /= sum;",
+                                      "if (s < 0.0) {\n            for (int k = 0; k < cnt; ++k) w[k] /= sum;"),
+    "resize_antialias_unstretched": ("const double d = ((double)k - t) * s;",
+                                     "const double d = ((double)k - t);"),
+    "resize_exclude_outside_no_renorm": ("if (sum != 0.0)\n            for (int k = 0; k < cnt; ++k) w[k] /= sum;",
+                                         "if (sum != sum)\n            for (int k = 0; k < cnt; ++k) w[k] /= sum;"),
+    "resize_crop_never_extrapolates": ("if (coord == RS_TF_CROP_AND_RESIZE && (x < 0.0 || x > (double)(n_in - 1))) return -1;",
+                                       "if (coord == RS_TF_CROP_AND_RESIZE && (x < -1e300)) return -1;"),
+    "resize_keep_policy_inverted": ("(keep_policy == RS_NOT_LARGER ? r < common : r > common)",
+                                    "(keep_policy == RS_NOT_LARGER ? r > common : r < common)"),
+    "resize_round_int_down": ("floor(common * (double)in_shape[d] + 0.5)",
+                              "floor(common * (double)in_shape[d])"),
+    "resize_roi_axes_reversed": ("roi_start[ax[i]] = roi[i];", "roi_start[ax[i]] = roi[na - 1 - i];"),
+    "resize_scaled_extent_rounded_up": ("out_shape[d] = (int64_t)floor(len);",
+                                        "out_shape[d] = (int64_t)ceil(len);"),
+    "resize_pytorch_half_pixel_single_not_zero": (
+        "return n_out > 1 ? (xr + 0.5) / scale - 0.5 : 0.0;", "return (xr + 0.5) / scale - 0.5;"),
+    "resize_cubic_antialias_linear_reach": ("const double reach = mode == OR_LINEAR ? 1.0 : 2.0;",
+                                            "const double reach = mode == OR_LINEAR ? 1.0 : 1.0;"),
+    "resize_nearest_ceil_as_floor": ("case RS_CEIL: return ceil(x);", "case RS_CEIL: return floor(x);"),
 }
 
 
@@ -78,6 +106,12 @@ def _run_pins():
         attempt(f"bilinear{case}", pins.test_deform_conv_is_a_contraction_of_bilinear_samples, case)
     for r, ac in ((2, 0), (2, 1), (3, 0), (3, 1)):
         attempt(f"affine_torch{r}{ac}", pins.test_affine_grid_matches_torch_cpu_fp64, r, ac)
+    for n in fixture_names("resize__"):
+        attempt(f"resize_page{n}", resize_pins.test_resize_page_example, n)
+    attempt("resize_repeat", resize_pins.test_nearest_double_asymmetric_is_repeat)
+    attempt("resize_1331", resize_pins.test_antialias_linear_half_is_1331_filter)
+    attempt("resize_crop", resize_pins.test_crop_and_resize_whole_roi_is_identity)
+    attempt("resize_extent", resize_pins.test_scale_output_extent_is_floored)
     return failed
 
 
