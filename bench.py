@@ -87,6 +87,8 @@ KERNEL_SOURCES = {
     "deform": ["gs_deform.cuh", "gs_deform_tc.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "deform_tc_nhwc": ["gs_deform_tc.cuh", "gs_copy.cuh", "gs_common.cuh", "gs_ptx.cuh",
                        "gs_internal.h"],
+    "vol_kernel": ["gs_vol.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "resize_kernel": ["gs_resize.cuh", "gs_common.cuh", "gs_internal.h"],
 }
 
 
@@ -200,8 +202,12 @@ class Case:
             self.host = {"theta": wl.as_dtype(inp["theta"], dtype), "X": wl.as_dtype(inp["X"], dtype)}
             self.size = [int(s) for s in inp["size"]]
             self.outputs = int(np.prod(self.size))
-            self.kernel_tag = (f"band_kernel<{DT_SHORT[dtype]},{self.mode}>" if w.r == 2 else
-                               f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},affine>")
+            if w.r == 2:
+                self.kernel_tag = f"band_kernel<{DT_SHORT[dtype]},{self.mode}>"
+            elif self.mode != "cubic":
+                self.kernel_tag = f"vol_kernel<{DT_SHORT[dtype]},{self.mode}>"
+            else:
+                self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},affine>"
         elif w.kind == "grid_sample":
             inp = wl.make_grid_sample_inputs(w, seed=seed)
             self.host = {"X": wl.as_dtype(inp["X"], dtype), "grid": wl.as_dtype(inp["grid"], dtype)}
@@ -216,6 +222,13 @@ class Case:
                     per = nbytes // slot
                     self.launches = 2 * (-(-w.x_shape[0] // per))   # copy + sample per chunk
                     self.kernel_tag = f"nhwc_sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
+        elif w.kind == "resize":
+            inp = wl.make_resize_inputs(w, seed=seed)
+            self.host = {"X": wl.as_dtype(inp["X"], dtype)}
+            self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
+            self.resize_kw = dict(scales=list(w.extra["scales"]), mode=self.mode,
+                                  antialias=w.extra["antialias"])
+            self.kernel_tag = f"resize_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
         else:
             inp = wl.make_deform_inputs(w, seed=seed)
             self.host = {k: wl.as_dtype(v, dtype) for k, v in inp.items()}
@@ -242,7 +255,7 @@ class Case:
         w = self.w
         if w.kind == "affine_sample":
             return self.size
-        if w.kind == "grid_sample":
+        if w.kind in ("grid_sample", "resize"):
             return list(w.x_shape[:2]) + list(w.out_spatial)
         N, C, H, W_ = w.x_shape
         return [N, w.oc, H, W_]
@@ -259,6 +272,8 @@ class Case:
             return self.gs.gs_grid_sample(d["X"], d["grid"], self.mode, w.padding_mode,
                                           w.align_corners, w.cubic_coeff_a, out=out,
                                           workspace=self.ws)
+        if w.kind == "resize":
+            return self.gs.gs_resize(d["X"], out=out, **self.resize_kw)
         return self.gs.gs_deform_conv(d["X"], d["W"], d["offset"], d["B"], d["mask"],
                                       kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
                                       dilations=w.dilations, group=w.group,
@@ -322,6 +337,12 @@ def time_e2e(case, steps, warmup):
                                         w.align_corners, w.cubic_coeff_a, out=out_host,
                                         streamer=streamer,
                                         workspace="auto" if case.ws is not None else None)
+    elif w.kind == "resize":
+        def fn(x, out):
+            return gs.gs_resize(x, out=out, **case.resize_kw)
+
+        def step():
+            streamer.run(fn, [pinned["X"]], out_host, [0])
     else:
         d = {k: torch.empty_like(v, device=case.device) for k, v in case.host.items()}
 
@@ -386,6 +407,8 @@ def oracle_sample(case, budget_s=12.0):
         elif w.kind == "grid_sample":
             Y = oracle.grid_sample(h["X"][sl], h["grid"][sl], case.mode, w.padding_mode,
                                    w.align_corners, w.cubic_coeff_a)
+        elif w.kind == "resize":
+            Y = oracle.resize(h["X"][sl], **case.resize_kw)
         else:
             Y = oracle.deform_conv(h["X"][sl], h["W"], h["offset"][sl], h["B"], h["mask"][sl],
                                    kernel_shape=w.kernel, pads=w.pads, strides=w.strides,
@@ -417,6 +440,10 @@ def workload_desc(case):
                 f"({w.x_shape[0]},{','.join(map(str, w.out_spatial))},{w.r}) {w.grid_dist}, "
                 f"{case.dtype}, {case.mode}, {w.padding_mode}, align_corners={w.align_corners}"
                 f"{via}")
+    if w.kind == "resize":
+        return (f"{case.name}: Resize {w.r}-D, X {tuple(w.x_shape)} ~ N(0,1) {case.dtype}, scales "
+                f"{tuple(w.extra['scales'])}, {case.mode}, half_pixel, "
+                f"antialias={w.extra['antialias']}, out {tuple(w.out_spatial)}")
     ws = getattr(case, "ws", None)
     via = (f"; gs_deform_conv_ws, channel-last workspace {ws.numel() / 2**20:.1f} MiB"
            if ws is not None else "")
@@ -480,7 +507,9 @@ def main():
                 ("gs2d_cubic", "float16", "nearest", True),
                 ("gs2d_small", "float32", None, False),
                 ("deform2d", "float32", None, False), ("deform2d", "bfloat16", None, False),
-                ("deform2d", "bfloat16", None, True)):
+                ("deform2d", "bfloat16", None, True),
+                ("resize2d_up", "float32", None, False), ("resize2d_up", "bfloat16", None, False),
+                ("resize2d_aa", "float32", None, False)):
             if (name, dt, mode, ws) == (args.workload, args.dtype, args.mode, args.workspace):
                 continue
             c2 = Case(name, dt, device, mode, workspace=ws)
@@ -540,6 +569,10 @@ def reference_arm(args, rank, world):
     elif w.kind == "grid_sample":
         inp = wl.make_grid_sample_inputs(w)
         case.host = {"X": wl.as_dtype(inp["X"], args.dtype), "grid": wl.as_dtype(inp["grid"], args.dtype)}
+    elif w.kind == "resize":
+        case.host = {"X": wl.as_dtype(wl.make_resize_inputs(w)["X"], args.dtype)}
+        case.resize_kw = dict(scales=list(w.extra["scales"]), mode=case.mode,
+                              antialias=w.extra["antialias"])
     else:
         inp = wl.make_deform_inputs(w)
         case.host = {k: wl.as_dtype(v, args.dtype) for k, v in inp.items()}

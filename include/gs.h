@@ -261,6 +261,78 @@ gs_status gs_deform_conv_ws(const void *X, const int64_t *x_shape, const void *W
                             const gs_deform_attrs *attrs, gs_dtype dt, void *workspace,
                             size_t workspace_bytes, void *Y, cudaStream_t stream);
 
+/*
+ * Resize -- Resize - 18 (Summary, Attributes, Inputs) on the same separable
+ * sampler.  Attribute values follow the operator's names.
+ */
+typedef enum {
+    GS_RS_HALF_PIXEL = 0, GS_RS_PYTORCH_HALF_PIXEL = 1, GS_RS_ALIGN_CORNERS = 2,
+    GS_RS_ASYMMETRIC = 3, GS_RS_TF_CROP_AND_RESIZE = 4
+} gs_resize_coord;
+typedef enum {
+    GS_RS_ROUND_PREFER_FLOOR = 0, GS_RS_ROUND_PREFER_CEIL = 1, GS_RS_FLOOR = 2, GS_RS_CEIL = 3
+} gs_resize_nearest;
+typedef enum { GS_RS_STRETCH = 0, GS_RS_NOT_LARGER = 1, GS_RS_NOT_SMALLER = 2 } gs_resize_keep;
+
+typedef struct {
+    gs_mode mode;                  /* nearest (the operator's default), linear, cubic      */
+    gs_resize_coord coord;         /* coordinate_transformation_mode, default half_pixel   */
+    gs_resize_nearest nearest_mode;/* default round_prefer_floor                           */
+    float cubic_coeff_a;           /* default -0.75                                        */
+    int exclude_outside;           /* 0 or 1                                               */
+    float extrapolation_value;     /* tf_crop_and_resize outside the input                 */
+    int antialias;                 /* 0 or 1: stretch linear / cubic by 1/scale downscaling */
+    gs_resize_keep keep_aspect_ratio_policy;   /* applies to sizes                         */
+} gs_resize_attrs;
+
+/*
+ * gs_resize_output_shape -- output extents of Resize (host only).
+ *
+ *   rank, x_shape  host: X's rank (1..8) and extents.
+ *   axes, naxes    host: the axes scales / sizes / roi refer to (negative
+ *                  counts from the back), or NULL / 0 for all axes in order.
+ *   scales         host float[naxes or rank], > 0, or NULL.  Output extent
+ *                  floor(in * (roi_end - roi_start) * scale).
+ *   sizes          host int64[naxes or rank], >= 0, or NULL.  Exactly one of
+ *                  scales and sizes.  keep_aspect_ratio_policy not_larger /
+ *                  not_smaller take one common scale, min / max of
+ *                  sizes[i] / in[axes[i]], and round scale * in halfway up.
+ *   roi            host float[2 * (naxes or rank)]: starts then ends,
+ *                  normalised; used only with tf_crop_and_resize (NULL: 0..1).
+ *   y_shape        host output, rank int64.
+ * Errors: GS_ERR_NULL, GS_ERR_RANK, GS_ERR_SHAPE (bad extents, repeated axis),
+ * GS_ERR_ATTR (bad attribute, scale <= 0, both or neither of scales/sizes).
+ */
+gs_status gs_resize_output_shape(int rank, const int64_t *x_shape, const int64_t *axes, int naxes,
+                                 const float *scales, const int64_t *sizes, const float *roi,
+                                 const gs_resize_attrs *attrs, int64_t *y_shape);
+
+/*
+ * gs_resize -- Resize - 18 of X into Y (device buffers, `dt` for both).
+ * Arguments as gs_resize_output_shape; Y must have that shape.
+ *
+ * Each axis maps output index o to x_original by the coordinate
+ * transformation (with "scales" the given scale is used and the resized
+ * length is n * scale, unfloored; with "sizes" scale = out / in), then takes
+ * its taps: nearest (nearest_mode), linear (floor(x), floor(x) + 1), cubic
+ * (floor(x) - 1 .. floor(x) + 2, Keys with cubic_coeff_a); antialias stretches
+ * the linear / cubic filter by 1/scale when downscaling and rescales the
+ * weights to sum 1; taps outside the axis read the edge value, or get weight
+ * 0 with the rest rescaled when exclude_outside = 1.  The output is the sum
+ * over the tensor product of the taps of the weights' product times X;
+ * tf_crop_and_resize writes extrapolation_value wherever x_original leaves
+ * [0, n - 1] on any axis.  Coordinates are formed in fp64; values accumulate
+ * in fp32.
+ *
+ * Axes whose map is the identity (same extent, scale 1, whole roi) are
+ * batched; the resized ones must be the last three or fewer
+ * (GS_ERR_UNSUPPORTED otherwise), with at most 64 taps per output index
+ * (antialias down to scale ~1/16 cubic, ~1/32 linear).
+ */
+gs_status gs_resize(const void *X, int rank, const int64_t *x_shape, const int64_t *axes,
+                    int naxes, const float *scales, const int64_t *sizes, const float *roi,
+                    const gs_resize_attrs *attrs, gs_dtype dt, void *Y, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gs_status_str(gs_status s);
 

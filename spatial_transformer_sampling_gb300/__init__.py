@@ -30,7 +30,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libgs.so")
 
 EXPORTED_SYMBOLS = ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
-                    "gs_status_str", "gs_device_status", "gs_version")
+                    "gs_resize", "gs_resize_output_shape", "gs_status_str", "gs_device_status",
+                    "gs_version")
 
 MODES = {"linear": 0, "bilinear": 0, "nearest": 1, "cubic": 2, "bicubic": 2}
 PADS = {"zeros": 0, "border": 1, "reflection": 2}
@@ -45,6 +46,20 @@ class GsError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
         super().__init__(f"{where}: {STATUS.get(status, status)} ({gs_status_str(status)})")
+
+
+class ResizeAttrs(ctypes.Structure):
+    """gs_resize_attrs (include/gs.h)."""
+    _fields_ = [("mode", ctypes.c_int), ("coord", ctypes.c_int), ("nearest_mode", ctypes.c_int),
+                ("cubic_coeff_a", ctypes.c_float), ("exclude_outside", ctypes.c_int),
+                ("extrapolation_value", ctypes.c_float), ("antialias", ctypes.c_int),
+                ("keep_aspect_ratio_policy", ctypes.c_int)]
+
+
+RESIZE_COORDS = {"half_pixel": 0, "pytorch_half_pixel": 1, "align_corners": 2, "asymmetric": 3,
+                 "tf_crop_and_resize": 4}
+RESIZE_NEAREST = {"round_prefer_floor": 0, "round_prefer_ceil": 1, "floor": 2, "ceil": 3}
+RESIZE_KEEP = {"stretch": 0, "not_larger": 1, "not_smaller": 2}
 
 
 class DeformAttrs(ctypes.Structure):
@@ -81,13 +96,19 @@ def load_library(path=None):
                                                 ci, ctypes.POINTER(ctypes.c_size_t)]
     L.gs_deform_conv_ws.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
                                     ctypes.POINTER(DeformAttrs), ci, vp, ctypes.c_size_t, vp, vp]
+    f32p = ctypes.POINTER(ctypes.c_float)
+    L.gs_resize_output_shape.argtypes = [ci, i64p, i64p, ci, f32p, i64p, f32p,
+                                         ctypes.POINTER(ResizeAttrs), i64p]
+    L.gs_resize.argtypes = [vp, ci, i64p, i64p, ci, f32p, i64p, f32p, ctypes.POINTER(ResizeAttrs),
+                            ci, vp, vp]
     L.gs_status_str.argtypes = [ci]
     L.gs_status_str.restype = ctypes.c_char_p
     L.gs_device_status.argtypes = [vp]
     L.gs_version.restype = ctypes.c_char_p
     for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
               "gs_grid_sample_ws", "gs_grid_sample_static", "gs_affine_sample", "gs_deform_conv",
-              "gs_deform_conv_workspace_size", "gs_deform_conv_ws", "gs_device_status"):
+              "gs_deform_conv_workspace_size", "gs_deform_conv_ws", "gs_device_status",
+              "gs_resize_output_shape", "gs_resize"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -329,6 +350,53 @@ def gs_deform_conv_ws(X, W, offset, B=None, mask=None, workspace="auto", **kw):
     return gs_deform_conv(X, W, offset, B, mask, workspace=workspace, **kw)
 
 
+def resize_attrs(mode="nearest", coordinate_transformation_mode="half_pixel",
+                 nearest_mode="round_prefer_floor", cubic_coeff_a=-0.75, exclude_outside=0,
+                 extrapolation_value=0.0, antialias=0, keep_aspect_ratio_policy="stretch"):
+    """gs_resize_attrs from the Resize operator's attribute names (the operator's defaults)."""
+    return ResizeAttrs(MODES[mode], RESIZE_COORDS[coordinate_transformation_mode],
+                       RESIZE_NEAREST[nearest_mode], float(cubic_coeff_a), int(exclude_outside),
+                       float(extrapolation_value), int(antialias),
+                       RESIZE_KEEP[keep_aspect_ratio_policy])
+
+
+def _resize_vectors(x_shape, scales, sizes, roi, axes):
+    f32 = lambda v: (ctypes.c_float * len(v))(*[float(x) for x in v]) if v is not None else None
+    ax = _i64(axes) if axes is not None else None
+    return (ax, 0 if axes is None else len(axes), f32(None if scales is None else list(scales)),
+            _i64(sizes) if sizes is not None else None, f32(None if roi is None else list(roi)))
+
+
+def gs_resize_output_shape(x_shape, scales=None, sizes=None, roi=None, axes=None, **attrs):
+    """Output extents of Resize (host computation in the library)."""
+    at = resize_attrs(**attrs)
+    ax, na, sc, sz, ro = _resize_vectors(x_shape, scales, sizes, roi, axes)
+    out = (ctypes.c_int64 * len(x_shape))()
+    _ok(load_library().gs_resize_output_shape(len(x_shape), _i64(x_shape), ax, na, sc, sz, ro,
+                                              ctypes.byref(at), out), "gs_resize_output_shape")
+    return tuple(int(v) for v in out)
+
+
+def gs_resize(X, scales=None, sizes=None, roi=None, axes=None, out=None, **attrs):
+    """Resize - 18 of a CUDA tensor; scales / sizes / roi / axes are host sequences and the
+    attributes take the operator's names (mode, coordinate_transformation_mode,
+    nearest_mode, cubic_coeff_a, exclude_outside, extrapolation_value, antialias,
+    keep_aspect_ratio_policy)."""
+    torch = _torch()
+    _check_tensors(X, out)
+    shape = gs_resize_output_shape(tuple(X.shape), scales, sizes, roi, axes, **attrs)
+    if out is None:
+        out = torch.empty(shape, dtype=X.dtype, device=X.device)
+    elif tuple(out.shape) != shape:
+        raise ValueError(f"out has shape {tuple(out.shape)}, Resize gives {shape}")
+    at = resize_attrs(**attrs)
+    ax, na, sc, sz, ro = _resize_vectors(X.shape, scales, sizes, roi, axes)
+    _ok(load_library().gs_resize(_ptr(X), X.dim(), _i64(X.shape), ax, na, sc, sz, ro,
+                                 ctypes.byref(at), _dtype_code(X), _ptr(out), _stream(X)),
+        "gs_resize")
+    return out
+
+
 def gs_device_status(device=None):
     """Synchronise the current stream and report the library's device error word."""
     torch = _torch()
@@ -346,9 +414,10 @@ class HostStreamer:
     """
 
     # With chunks=None the batch is cut into chunks of about this many input
-    # bytes (whole images): the first chunk's upload and the last chunk's
-    # download are not overlapped with anything, so smaller chunks cost less.
-    CHUNK_BYTES = 4 << 20
+    # bytes (whole images).  The first chunk's upload and the last chunk's
+    # download overlap nothing, which favours small chunks; each chunk also
+    # costs host time to enqueue, which favours large ones.
+    CHUNK_BYTES = 16 << 20
 
     def __init__(self, device=None, chunks=None):
         torch = _torch()

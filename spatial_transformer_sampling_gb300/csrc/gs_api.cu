@@ -188,7 +188,188 @@ gs_status check_deform(const void *X, const int64_t *x_shape, const void *W, int
 
 }  // namespace
 
+namespace {
+
+// Resize - 18: output extents and per-axis coordinate parameters.
+constexpr int kRsMaxRank = 8;
+constexpr int64_t kRsMaxExtent = int64_t(1) << 24;
+
+struct ResizePlan {
+    int rank;
+    int64_t in[kRsMaxRank], out[kRsMaxRank];
+    double scale[kRsMaxRank], lres[kRsMaxRank], r0[kRsMaxRank], r1[kRsMaxRank];
+};
+
+gs_status resize_plan(int rank, const int64_t *x_shape, const int64_t *axes, int naxes,
+                      const float *scales, const int64_t *sizes, const float *roi,
+                      const gs_resize_attrs *at, ResizePlan *P) {
+    if (!x_shape || !at) return GS_ERR_NULL;
+    if (rank < 1 || rank > kRsMaxRank) return GS_ERR_RANK;
+    if ((scales == nullptr) == (sizes == nullptr)) return GS_ERR_ATTR;
+    if ((int)at->mode < GS_LINEAR || (int)at->mode > GS_CUBIC) return GS_ERR_ATTR;
+    if ((int)at->coord < GS_RS_HALF_PIXEL || (int)at->coord > GS_RS_TF_CROP_AND_RESIZE)
+        return GS_ERR_ATTR;
+    if ((int)at->nearest_mode < GS_RS_ROUND_PREFER_FLOOR || (int)at->nearest_mode > GS_RS_CEIL)
+        return GS_ERR_ATTR;
+    if ((int)at->keep_aspect_ratio_policy < GS_RS_STRETCH ||
+        (int)at->keep_aspect_ratio_policy > GS_RS_NOT_SMALLER)
+        return GS_ERR_ATTR;
+    if ((at->exclude_outside != 0 && at->exclude_outside != 1) ||
+        (at->antialias != 0 && at->antialias != 1) || !isfinite(at->cubic_coeff_a))
+        return GS_ERR_ATTR;
+    if (naxes < 0 || naxes > rank || (naxes > 0 && !axes)) return GS_ERR_SHAPE;
+    const int na = naxes > 0 ? naxes : rank;
+    int ax[kRsMaxRank];
+    bool seen[kRsMaxRank] = {};
+    for (int i = 0; i < na; ++i) {
+        int64_t d = naxes > 0 ? axes[i] : i;
+        if (d < 0) d += rank;
+        if (d < 0 || d >= rank || seen[d]) return GS_ERR_SHAPE;
+        seen[d] = true;
+        ax[i] = (int)d;
+    }
+    P->rank = rank;
+    for (int d = 0; d < rank; ++d) {
+        if (x_shape[d] < 0 || x_shape[d] > kRsMaxExtent) return GS_ERR_SHAPE;
+        P->in[d] = P->out[d] = x_shape[d];
+        P->scale[d] = 1.0;
+        P->lres[d] = (double)x_shape[d];
+        P->r0[d] = 0.0;
+        P->r1[d] = 1.0;
+    }
+    if (roi && at->coord == GS_RS_TF_CROP_AND_RESIZE) {
+        for (int i = 0; i < na; ++i) {
+            if (!isfinite(roi[i]) || !isfinite(roi[na + i])) return GS_ERR_ATTR;
+            P->r0[ax[i]] = roi[i];
+            P->r1[ax[i]] = roi[na + i];
+        }
+    }
+    if (scales) {
+        for (int i = 0; i < na; ++i) {
+            const int d = ax[i];
+            const double sc = scales[i];
+            if (!(sc > 0.0) || !isfinite(sc)) return GS_ERR_ATTR;
+            const double len = (double)P->in[d] * (P->r1[d] - P->r0[d]) * sc;
+            if (!(len >= 0.0) || len >= (double)(kRsMaxExtent + 1)) return GS_ERR_SHAPE;
+            P->out[d] = (int64_t)floor(len);
+            P->scale[d] = sc;
+            P->lres[d] = len;
+        }
+        return GS_OK;
+    }
+    double common = 0.0;
+    if (at->keep_aspect_ratio_policy != GS_RS_STRETCH) {
+        for (int i = 0; i < na; ++i) {
+            if (P->in[ax[i]] == 0) return GS_ERR_SHAPE;
+            const double q = (double)sizes[i] / (double)P->in[ax[i]];
+            if (i == 0 || (at->keep_aspect_ratio_policy == GS_RS_NOT_LARGER ? q < common : q > common))
+                common = q;
+        }
+    }
+    for (int i = 0; i < na; ++i) {
+        const int d = ax[i];
+        if (sizes[i] < 0 || sizes[i] > kRsMaxExtent) return GS_ERR_SHAPE;
+        const double o = at->keep_aspect_ratio_policy == GS_RS_STRETCH
+                             ? (double)sizes[i]
+                             : floor(common * (double)P->in[d] + 0.5);
+        if (!(o >= 0.0) || o > (double)kRsMaxExtent) return GS_ERR_SHAPE;
+        P->out[d] = (int64_t)o;
+        P->scale[d] = P->in[d] > 0 ? o / (double)P->in[d] : 1.0;
+        P->lres[d] = o;
+    }
+    return GS_OK;
+}
+
+// Taps per output index on one axis: 1 (nearest), else the offsets k0 .. 1-k0
+// from floor(x) where the filter, stretched by 1/aa when antialiasing a
+// downscale, can be nonzero (linear reaches 1, cubic 2).
+void resize_taps_per_axis(const gs_resize_attrs *at, double scale, gs::ResizeAxis *A) {
+    A->aa_scale = (at->antialias && at->mode != GS_NEAREST && scale < 1.0) ? scale : 1.0;
+    if (at->mode == GS_NEAREST) {
+        A->k0 = 0;
+        A->taps = 1;
+        return;
+    }
+    const double reach = at->mode == GS_LINEAR ? 1.0 : 2.0;
+    const double k0 = floor(-reach / A->aa_scale) + 1.0;
+    A->k0 = k0 < -1.0e6 ? -1000000 : (int)k0;
+    A->taps = 2 - 2 * A->k0;
+}
+
+}  // namespace
+
 extern "C" {
+
+gs_status gs_resize_output_shape(int rank, const int64_t *x_shape, const int64_t *axes, int naxes,
+                                 const float *scales, const int64_t *sizes, const float *roi,
+                                 const gs_resize_attrs *attrs, int64_t *y_shape) {
+    if (!y_shape) return GS_ERR_NULL;
+    ResizePlan P;
+    const gs_status st = resize_plan(rank, x_shape, axes, naxes, scales, sizes, roi, attrs, &P);
+    if (st != GS_OK) return st;
+    for (int d = 0; d < rank; ++d) y_shape[d] = P.out[d];
+    return GS_OK;
+}
+
+gs_status gs_resize(const void *X, int rank, const int64_t *x_shape, const int64_t *axes,
+                    int naxes, const float *scales, const int64_t *sizes, const float *roi,
+                    const gs_resize_attrs *attrs, gs_dtype dt, void *Y, cudaStream_t stream) {
+    ResizePlan P;
+    gs_status st = resize_plan(rank, x_shape, axes, naxes, scales, sizes, roi, attrs, &P);
+    if (st != GS_OK) return st;
+    if (!dtype_ok(dt)) return GS_ERR_DTYPE;
+    bool empty_out = false, empty_in = false;
+    for (int d = 0; d < rank; ++d) {
+        empty_out = empty_out || P.out[d] == 0;
+        empty_in = empty_in || P.in[d] == 0;
+    }
+    if (empty_out) return GS_OK;
+    if (empty_in) return GS_ERR_SHAPE;   // nothing to sample from
+    if (!X || !Y) return GS_ERR_NULL;
+    if (!aligned(X, elem_size(dt)) || !aligned(Y, elem_size(dt))) return GS_ERR_ALIGN;
+    // identity axes (same extent, scale 1, whole roi) in front of the first
+    // resized one become slices
+    auto identity = [&](int d) {
+        return P.out[d] == P.in[d] && P.scale[d] == 1.0 && P.r0[d] == 0.0 && P.r1[d] == 1.0;
+    };
+    int f = 0;
+    while (f < rank - 1 && identity(f)) ++f;
+    const int R = rank - f;
+    if (R > 3) return GS_ERR_UNSUPPORTED;
+    gs::ResizeArgs a;
+    a.r = R;
+    a.B = 1;
+    for (int d = 0; d < f; ++d) a.B *= P.in[d];
+    a.mode = (int)attrs->mode;
+    a.coord = (int)attrs->coord;
+    a.nearest_mode = (int)attrs->nearest_mode;
+    a.a = attrs->cubic_coeff_a;
+    a.exclude_outside = attrs->exclude_outside;
+    a.extrapolation_value = attrs->extrapolation_value;
+    for (int i = 0; i < 3; ++i) {
+        gs::ResizeAxis &A = a.ax[i];
+        const int d = f + i - (3 - R);
+        if (i < 3 - R) {   // unit axis
+            A.n_in = A.n_out = 1;
+            A.scale = A.length_resized = A.roi_end = A.aa_scale = 1.0;
+            A.roi_start = 0.0;
+            A.k0 = 0;
+            A.taps = 1;
+            continue;
+        }
+        A.n_in = (int)P.in[d];
+        A.n_out = (int)P.out[d];
+        A.scale = P.scale[d];
+        A.length_resized = P.lres[d];
+        A.roi_start = P.r0[d];
+        A.roi_end = P.r1[d];
+        resize_taps_per_axis(attrs, P.scale[d], &A);
+        if (A.taps > gs::kRsMaxTapsHost) return GS_ERR_UNSUPPORTED;
+    }
+    return dispatch(dt, [&](auto tag) {
+        return gs::launch_resize<decltype(tag)>(X, Y, a, stream);
+    });
+}
 
 gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *size,
                          int align_corners, void *grid, cudaStream_t stream) {

@@ -40,6 +40,35 @@ struct DeformArgs {
     unsigned *err;       // device error word (bounded waits record timeouts here)
 };
 
+// Resize (Resize - 18): coordinate maps and nearest rounding.
+enum { RS_HALF_PIXEL = 0, RS_PYTORCH_HALF_PIXEL = 1, RS_ALIGN_CORNERS = 2, RS_ASYMMETRIC = 3,
+       RS_TF_CROP_AND_RESIZE = 4 };
+enum { RS_ROUND_PREFER_FLOOR = 0, RS_ROUND_PREFER_CEIL = 1, RS_FLOOR = 2, RS_CEIL = 3 };
+
+// One resized axis.  taps: taps per output index (1 nearest, 2 linear,
+// 4 cubic, more when antialiasing a downscale); k0: offset of the first tap
+// from floor(x) (the last is 1 - k0); aa_scale: the scale the filter is
+// stretched by (1 unless antialiasing a downscale).
+struct ResizeAxis {
+    int n_in, n_out;
+    double scale, length_resized, roi_start, roi_end, aa_scale;
+    int k0, taps;
+};
+
+constexpr int kRsMaxTapsHost = 64;   // taps per output index the Resize kernel holds
+
+// Arguments of the Resize kernel: r trailing resized axes in ax[3-r..2]
+// (ax[0..2-r] are unit axes), B slices made of the leading axes.
+struct ResizeArgs {
+    ResizeAxis ax[3];
+    int64_t B;
+    int r;
+    int mode, coord, nearest_mode;
+    double a;
+    int exclude_outside;
+    float extrapolation_value;
+};
+
 // Per-dtype launchers; T is float, __half or __nv_bfloat16.  Each enqueues on
 // `s` and returns the launch error (cudaSuccess when fine).
 // `ws`, `ws_bytes`: optional device workspace for the channel-last GridSample
@@ -68,5 +97,7 @@ cudaError_t launch_deform_ws(const void *X, const void *W, const void *offset, c
                              size_t ws_bytes, cudaStream_t s);
 template <typename T>
 size_t deform_ws_bytes(const DeformArgs &args);
+template <typename T>
+cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &args, cudaStream_t s);
 
 }  // namespace gs

@@ -1,6 +1,7 @@
 // gs_kernels_f32.cu -- float instantiations of the libgs kernels (one
 // translation unit per dtype so the build compiles them in parallel).
 #include "gs_deform.cuh"
+#include "gs_resize.cuh"
 #include "gs_sample.cuh"
 
 namespace gs {
@@ -16,4 +17,5 @@ template cudaError_t launch_deform_ws<float>(const void *, const void *, const v
                                              const void *, void *, const DeformArgs &, void *,
                                              size_t, cudaStream_t);
 template size_t deform_ws_bytes<float>(const DeformArgs &);
+template cudaError_t launch_resize<float>(const void *, void *, const ResizeArgs &, cudaStream_t);
 }  // namespace gs

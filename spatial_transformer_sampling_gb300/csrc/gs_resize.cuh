@@ -1,0 +1,368 @@
+// gs_resize.cuh -- Resize (Resize - 18) on the separable sampler.
+//
+// Resize maps every output axis on its own: output index o -> source
+// coordinate x (coordinate_transformation_mode), then taps and 1-D weights
+// (nearest with nearest_mode, linear, Keys cubic with cubic_coeff_a; with
+// antialias the linear / cubic filter is stretched by 1/scale when
+// downscaling and renormalised; exclude_outside drops taps outside the axis
+// and renormalises; other taps outside the axis read the edge value).  The
+// value is the sum over the tensor product of the taps of the product of
+// the weights times X.  tf_crop_and_resize puts extrapolation_value wherever a
+// coordinate leaves the input on any axis.
+//
+// The host folds every axis whose map is the identity into a batch axis of B
+// slices, leaving r = 1, 2 or 3 trailing resized axes.  A block owns a tile
+// of at most 256 output positions (tz x ty x tx) and a range of slices.  It
+// first tabulates the taps of its tile's indices along each axis in shared
+// memory (source coordinates in fp64, the precision the operator's
+// definition is written in, so the tap choice of nearest and the crop test
+// are exact), then each thread takes one position and sweeps the slices,
+// holding its taps in registers when every axis has a fixed tap count (1, 2
+// or 4) and reading them from shared memory otherwise (antialias).
+#pragma once
+
+#include <algorithm>
+
+#include "gs_common.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kRsThreads = 256;
+constexpr int kRsMaxTaps = kRsMaxTapsHost;   // per axis (antialias at scale >= ~1/16 cubic, ~1/32 linear)
+
+// Output tile of a block.
+struct ResizeTile {
+    int t[3];        // tile extents, outermost axis first (1 for unused axes)
+    int tiles[3];    // tiles along each axis
+};
+
+__device__ __forceinline__ double rs_keys(double s, double a) {
+    s = fabs(s);
+    if (s <= 1.0) return ((a + 2.0) * s - (a + 3.0)) * s * s + 1.0;
+    if (s < 2.0) return ((a * s - 5.0 * a) * s + 8.0 * a) * s - 4.0 * a;
+    return 0.0;
+}
+
+// Taps of output index o on axis A: indices clamped to the axis (edge values),
+// weights; returns the count, or -1 when the element takes
+// extrapolation_value.  The count depends only on the axis (the host sets it
+// with A.k0 and A.taps), so every entry of a table has the same length.
+static __device__ int rs_axis_taps(int o, const ResizeAxis &A, const ResizeArgs &p, int *idx, float *w) {
+    const double xr = (double)o;
+    double x;
+    switch (p.coord) {
+        case RS_PYTORCH_HALF_PIXEL:
+            x = A.n_out > 1 ? (xr + 0.5) / A.scale - 0.5 : 0.0;
+            break;
+        case RS_ALIGN_CORNERS:
+            x = A.length_resized > 1.0 ? xr * (double)(A.n_in - 1) / (A.length_resized - 1.0) : 0.0;
+            break;
+        case RS_ASYMMETRIC:
+            x = xr / A.scale;
+            break;
+        case RS_TF_CROP_AND_RESIZE:
+            x = A.n_out > 1 ? A.roi_start * (double)(A.n_in - 1) +
+                                  xr * (A.roi_end - A.roi_start) * (double)(A.n_in - 1) /
+                                      (double)(A.n_out - 1)
+                            : 0.5 * (A.roi_start + A.roi_end) * (double)(A.n_in - 1);
+            break;
+        default:   // half_pixel
+            x = (xr + 0.5) / A.scale - 0.5;
+            break;
+    }
+    if (p.coord == RS_TF_CROP_AND_RESIZE && (x < 0.0 || x > (double)(A.n_in - 1))) return -1;
+    // keep the integer conversions defined for coordinates far outside
+    x = fmin(fmax(x, -1.0e9), 1.0e9);
+    const int n = A.n_in;
+    int cnt;
+    double wd[kRsMaxTaps];
+    if (p.mode == MODE_NEAREST) {
+        double r;
+        switch (p.nearest_mode) {
+            case RS_ROUND_PREFER_CEIL: r = floor(x + 0.5); break;
+            case RS_FLOOR: r = floor(x); break;
+            case RS_CEIL: r = ceil(x); break;
+            default: r = ceil(x - 0.5); break;   // round_prefer_floor
+        }
+        idx[0] = (int)r;
+        wd[0] = 1.0;
+        cnt = 1;
+    } else {
+        const double f = floor(x), t = x - f;
+        const int i0 = (int)f;
+        const double s = A.aa_scale;   // scale when antialiasing a downscale, else 1
+        const int k0 = A.k0;           // first tap offset from floor(x); the last is 1 - k0
+        cnt = 1 - 2 * k0 + 1;
+        double sum = 0.0;
+        for (int k = 0; k < cnt; ++k) {
+            const double d = ((double)(k0 + k) - t) * s;
+            const double wk = p.mode == MODE_LINEAR ? fmax(0.0, 1.0 - fabs(d)) : rs_keys(d, p.a);
+            idx[k] = i0 + k0 + k;
+            wd[k] = wk;
+            sum += wk;
+        }
+        if (s < 1.0)
+            for (int k = 0; k < cnt; ++k) wd[k] /= sum;
+    }
+    if (p.exclude_outside) {
+        double sum = 0.0;
+        for (int k = 0; k < cnt; ++k) {
+            if (idx[k] < 0 || idx[k] > n - 1) wd[k] = 0.0;
+            sum += wd[k];
+        }
+        if (sum != 0.0)
+            for (int k = 0; k < cnt; ++k) wd[k] /= sum;
+    }
+    for (int k = 0; k < cnt; ++k) {
+        idx[k] = idx[k] < 0 ? 0 : (idx[k] > n - 1 ? n - 1 : idx[k]);
+        w[k] = (float)wd[k];
+    }
+    return cnt;
+}
+
+// One output value of one slice from per-axis taps (separable sum, innermost
+// axis first).  K: taps per axis when fixed (1, 2, 4), 0 when read from the
+// shared tables with counts cnt[].
+template <typename T, int R, int K>
+__device__ __forceinline__ float rs_value(const T *__restrict__ Xs, const ResizeArgs &p,
+                                          const int (*ti)[K > 0 ? K : 1],
+                                          const float (*tw)[K > 0 ? K : 1],
+                                          const int *const *si, const float *const *sw,
+                                          const int *cnt) {
+    const int W = p.ax[2].n_in, H = p.ax[1].n_in;
+    auto row_sum = [&](const T *row) {
+        float s = 0.0f;
+        if constexpr (K > 0) {
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) s = fmaf(tw[2][kx], IO<T>::ld(row + ti[2][kx]), s);
+        } else {
+            for (int kx = 0; kx < cnt[2]; ++kx) s = fmaf(sw[2][kx], IO<T>::ld(row + si[2][kx]), s);
+        }
+        return s;
+    };
+    auto plane_sum = [&](const T *plane) {
+        if constexpr (R == 1) {
+            return row_sum(plane);
+        } else {
+            float s = 0.0f;
+            if constexpr (K > 0) {
+#pragma unroll
+                for (int ky = 0; ky < K; ++ky)
+                    s = fmaf(tw[1][ky], row_sum(plane + (int64_t)ti[1][ky] * W), s);
+            } else {
+                for (int ky = 0; ky < cnt[1]; ++ky)
+                    s = fmaf(sw[1][ky], row_sum(plane + (int64_t)si[1][ky] * W), s);
+            }
+            return s;
+        }
+    };
+    if constexpr (R <= 2) {
+        return plane_sum(Xs);
+    } else {
+        float s = 0.0f;
+        const int64_t HW = (int64_t)H * W;
+        if constexpr (K > 0) {
+#pragma unroll
+            for (int kz = 0; kz < K; ++kz) s = fmaf(tw[0][kz], plane_sum(Xs + ti[0][kz] * HW), s);
+        } else {
+            for (int kz = 0; kz < cnt[0]; ++kz) s = fmaf(sw[0][kz], plane_sum(Xs + si[0][kz] * HW), s);
+        }
+        return s;
+    }
+}
+
+// Grid: blockIdx.x = tile, blockIdx.y = slice chunk.  Axes are stored in
+// p.ax[0..2] outermost first; for R < 3 the leading entries are unit axes.
+template <typename T, int R, int K>
+__global__ void __launch_bounds__(kRsThreads)
+resize_kernel(const T *__restrict__ X, T *__restrict__ Y, const ResizeArgs p, const ResizeTile tl,
+              int slices_per_block) {
+    extern __shared__ __align__(16) unsigned char rs_smem[];
+    const int tid = threadIdx.x;
+    int tile = blockIdx.x;
+    int tc[3];
+    for (int d = 2; d >= 0; --d) {
+        tc[d] = tile % tl.tiles[d];
+        tile /= tl.tiles[d];
+    }
+    int o0[3], ext[3];
+    for (int d = 0; d < 3; ++d) {
+        o0[d] = tc[d] * tl.t[d];
+        ext[d] = min(tl.t[d], p.ax[d].n_out - o0[d]);
+    }
+    // shared tables: per axis, tile entries x taps (index, weight), plus a flag
+    int *s_idx[3];
+    float *s_w[3];
+    int *s_flag[3];
+    {
+        unsigned char *q = rs_smem;
+        for (int d = 0; d < 3; ++d) {
+            const int entries = tl.t[d] * p.ax[d].taps;
+            s_idx[d] = reinterpret_cast<int *>(q);
+            q += (size_t)entries * 4;
+            s_w[d] = reinterpret_cast<float *>(q);
+            q += (size_t)entries * 4;
+            s_flag[d] = reinterpret_cast<int *>(q);
+            q += (size_t)tl.t[d] * 4;
+        }
+    }
+    for (int d = 0; d < 3; ++d) {
+        for (int e = tid; e < ext[d]; e += kRsThreads) {
+            const int taps = p.ax[d].taps;
+            if (d < 3 - R) {   // a unit axis: index 0, weight 1
+                s_idx[d][e] = 0;
+                s_w[d][e] = 1.0f;
+                s_flag[d][e] = 0;
+                continue;
+            }
+            int ib[kRsMaxTaps];
+            float wb[kRsMaxTaps];
+            const int c = rs_axis_taps(o0[d] + e, p.ax[d], p, ib, wb);
+            s_flag[d][e] = c < 0 ? 1 : 0;
+            for (int k = 0; k < taps; ++k) {
+                s_idx[d][e * taps + k] = c < 0 ? 0 : ib[k];
+                s_w[d][e * taps + k] = c < 0 ? 0.0f : wb[k];
+            }
+        }
+    }
+    __syncthreads();
+
+    // this thread's position in the tile
+    const int tx = tl.t[2], ty = tl.t[1];
+    const int pz = tid / (tx * ty), py = (tid / tx) % ty, px = tid % tx;
+    const int pe[3] = {pz, py, px};
+    if (pz >= tl.t[0] || pz >= ext[0] || py >= ext[1] || px >= ext[2]) return;
+    const bool extrap = s_flag[0][pz] | s_flag[1][py] | s_flag[2][px];
+
+    constexpr int KK = K > 0 ? K : 1;
+    int ti[3][KK];
+    float tw[3][KK];
+    const int *si[3];
+    const float *sw[3];
+    int cnt[3];
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        cnt[d] = p.ax[d].taps;
+        si[d] = s_idx[d] + pe[d] * cnt[d];
+        sw[d] = s_w[d] + pe[d] * cnt[d];
+        if constexpr (K > 0) {
+            if (d >= 3 - R) {   // resized axes hold K taps each
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    ti[d][k] = si[d][k];
+                    tw[d][k] = sw[d][k];
+                }
+            }
+        }
+    }
+
+    const int64_t in_slice = (int64_t)p.ax[0].n_in * p.ax[1].n_in * p.ax[2].n_in;
+    const int64_t out_slice = (int64_t)p.ax[0].n_out * p.ax[1].n_out * p.ax[2].n_out;
+    const int64_t oidx = ((int64_t)(o0[0] + pz) * p.ax[1].n_out + (o0[1] + py)) * p.ax[2].n_out +
+                         (o0[2] + px);
+    const int64_t b0 = (int64_t)blockIdx.y * slices_per_block;
+    const int64_t b1 = min((int64_t)p.B, b0 + slices_per_block);
+    const T *Xs = X + b0 * in_slice;
+    T *Yp = Y + b0 * out_slice + oidx;
+    if (extrap) {
+        const T v = IO<T>::st(p.extrapolation_value);
+        for (int64_t b = b0; b < b1; ++b, Yp += out_slice) *Yp = v;
+        return;
+    }
+    constexpr int KR = K == 0 ? 0 : (R == 1 ? K : (R == 2 ? K * K : K * K * K));
+    if constexpr (K > 0 && KR <= 16) {
+        // the tap tuple flattened: offsets inside a slice and weight products,
+        // row-major over the axes (the order of the operator's sum)
+        int off[KR];
+        float wt[KR];
+#pragma unroll
+        for (int t = 0; t < KR; ++t) {
+            int rem = t;
+            const int kx = rem % K;
+            rem /= K;
+            const int ky = R >= 2 ? rem % K : 0;
+            const int kz = R >= 3 ? rem / K : 0;
+            const int iz = R >= 3 ? ti[0][kz] : 0, iy = R >= 2 ? ti[1][ky] : 0;
+            off[t] = (iz * p.ax[1].n_in + iy) * p.ax[2].n_in + ti[2][kx];
+            wt[t] = (R >= 3 ? tw[0][kz] : 1.0f) * (R >= 2 ? tw[1][ky] : 1.0f) * tw[2][kx];
+        }
+        // four independent slices per step: all their loads are in flight together
+        int64_t b = b0;
+        for (; b + 4 <= b1; b += 4) {
+            float acc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[u] = 0.0f;
+#pragma unroll
+                for (int t = 0; t < KR; ++t)
+                    acc[u] = fmaf(wt[t], IO<T>::ld(Xs + u * in_slice + off[t]), acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) Yp[u * out_slice] = IO<T>::st(acc[u]);
+            Xs += 4 * in_slice;
+            Yp += 4 * out_slice;
+        }
+        for (; b < b1; ++b) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int t = 0; t < KR; ++t) acc = fmaf(wt[t], IO<T>::ld(Xs + off[t]), acc);
+            *Yp = IO<T>::st(acc);
+            Xs += in_slice;
+            Yp += out_slice;
+        }
+    } else {
+        for (int64_t b = b0; b < b1; ++b) {
+            *Yp = IO<T>::st(rs_value<T, R, K>(Xs, p, ti, tw, si, sw, cnt));
+            Xs += in_slice;
+            Yp += out_slice;
+        }
+    }
+}
+
+template <typename T, int R>
+static cudaError_t launch_resize_r(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s) {
+    // tile: up to 256 positions, innermost axis widest
+    ResizeTile tl;
+    const int n2 = p.ax[2].n_out, n1 = p.ax[1].n_out, n0 = p.ax[0].n_out;
+    tl.t[2] = min(n2, 32);
+    tl.t[1] = min(n1, kRsThreads / tl.t[2]);
+    tl.t[0] = min(n0, kRsThreads / (tl.t[2] * tl.t[1]));
+    for (int d = 0; d < 3; ++d) {
+        const int n = p.ax[d].n_out;
+        tl.tiles[d] = (n + tl.t[d] - 1) / tl.t[d];
+    }
+    const int64_t tiles = (int64_t)tl.tiles[0] * tl.tiles[1] * tl.tiles[2];
+    // slices per block: enough blocks for several waves, at most 64 slices each
+    int64_t per = 64;
+    while (per > 1 && tiles * ((p.B + per - 1) / per) < 8 * 152) per >>= 1;
+    per = std::max<int64_t>(per, (p.B + 65534) / 65535);   // gridDim.y limit
+    const int64_t chunks = (p.B + per - 1) / per;
+    if (tiles > 0x7fffffffLL || chunks > 65535) return cudaErrorInvalidConfiguration;
+    size_t smem = 0;
+    for (int d = 0; d < 3; ++d) smem += (size_t)tl.t[d] * (p.ax[d].taps * 8 + 4);
+    const dim3 grid((unsigned)tiles, (unsigned)chunks);
+    // one fixed tap count on every resized axis: taps in registers
+    const int taps = p.ax[2].taps;
+    bool fixed = taps == 1 || taps == 2 || taps == 4;
+    for (int d = 3 - R; d < 3; ++d) fixed = fixed && p.ax[d].taps == taps;
+    if (fixed && taps == 1) {
+        resize_kernel<T, R, 1><<<grid, kRsThreads, smem, s>>>((const T *)X, (T *)Y, p, tl, (int)per);
+    } else if (fixed && taps == 2) {
+        resize_kernel<T, R, 2><<<grid, kRsThreads, smem, s>>>((const T *)X, (T *)Y, p, tl, (int)per);
+    } else if (fixed && taps == 4) {
+        resize_kernel<T, R, 4><<<grid, kRsThreads, smem, s>>>((const T *)X, (T *)Y, p, tl, (int)per);
+    } else {
+        resize_kernel<T, R, 0><<<grid, kRsThreads, smem, s>>>((const T *)X, (T *)Y, p, tl, (int)per);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s) {
+    if (p.r == 1) return launch_resize_r<T, 1>(X, Y, p, s);
+    if (p.r == 2) return launch_resize_r<T, 2>(X, Y, p, s);
+    return launch_resize_r<T, 3>(X, Y, p, s);
+}
+
+}  // namespace gs

@@ -26,6 +26,11 @@ stand-ins, one seed per workload, ``1000 + index``):
                  N(0, 0.05), B (64) ~ N(0,1), pads 1, stride 1, group 1,
                  offset_group 1, offset (8,18,64,64) ~ N(0,1),
                  mask (8,9,64,64) = sigmoid(N(0,1)); fp32 and bf16.
+  5 resize2d_up  Resize (on the same separable sampler), 2x bilinear upscale,
+                 half_pixel: X (16,64,128,128) ~ N(0,1), scales (1,1,2,2);
+                 fp32 and bf16.
+  6 resize2d_aa  Resize, antialiased bilinear 2x downscale, half_pixel:
+                 X (16,64,256,256) ~ N(0,1), scales (1,1,0.5,0.5); fp32.
 
 The second argument of N(., .) is the standard deviation.
 """
@@ -40,7 +45,7 @@ WORKLOADS = {}
 class Workload:
     index: int
     name: str
-    kind: str                      # "grid_sample" | "affine_sample" | "deform_conv"
+    kind: str                      # "grid_sample" | "affine_sample" | "deform_conv" | "resize"
     r: int
     x_shape: tuple
     out_spatial: tuple = ()
@@ -82,6 +87,10 @@ _reg(Workload(2, "gs2d_cubic", "grid_sample", 2, (16, 64, 256, 256), (256, 256),
 _reg(Workload(3, "stn3d", "affine_sample", 3, (4, 16, 64, 64, 64), (64, 64, 64)))
 _reg(Workload(4, "deform2d", "deform_conv", 2, (8, 64, 64, 64), oc=64,
               dtypes=("float32", "bfloat16")))
+_reg(Workload(5, "resize2d_up", "resize", 2, (16, 64, 128, 128), (256, 256),
+              dtypes=("float32", "bfloat16"), extra={"scales": (1.0, 1.0, 2.0, 2.0), "antialias": 0}))
+_reg(Workload(6, "resize2d_aa", "resize", 2, (16, 64, 256, 256), (128, 128),
+              extra={"scales": (1.0, 1.0, 0.5, 0.5), "antialias": 1}))
 
 
 def rng(seed):
@@ -142,6 +151,12 @@ def make_deform_inputs(w, seed=None, x_shape=None, oc=None, kernel=None):
     offset = g.normal(0.0, 1.0, size=(N, w.offset_group * kh * kw * 2, oh, ow))
     mask = 1.0 / (1.0 + np.exp(-g.normal(0.0, 1.0, size=(N, w.offset_group * kh * kw, oh, ow))))
     return {"X": X, "W": Wt, "B": B, "offset": offset, "mask": mask}
+
+
+def make_resize_inputs(w, seed=None, x_shape=None):
+    """X for a Resize workload (the scales and attributes are in w)."""
+    g = rng(w.seed if seed is None else seed)
+    return {"X": draw(g, w.x_dist, tuple(x_shape or w.x_shape))}
 
 
 def as_dtype(a, dtype):

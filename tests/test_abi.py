@@ -146,3 +146,65 @@ def test_deform_conv_workspace_size_queries(L):
 def test_deform_conv_null_attrs(L):
     assert L.gs_deform_conv(FAKE, _i64([1, 1, 4, 4]), FAKE, 1, FAKE, None, None, None, 0, FAKE,
                             None) == 1
+
+
+# ------------------------------------------------------------------ Resize host logic
+
+def _resize_shape_lib(x_shape, **kw):
+    return gs.gs_resize_output_shape(tuple(x_shape), **kw)
+
+
+@pytest.mark.parametrize("case", [
+    dict(x=(1, 1, 4, 4), scales=[1, 1, 0.6, 0.6]),
+    dict(x=(1, 1, 2, 4), scales=[1, 1, 0.6, 0.6]),
+    dict(x=(2, 3, 7, 10), scales=[1, 1, 0.5, 1.55]),
+    dict(x=(1, 1, 2, 2), sizes=[7, 8], axes=[2, 3], keep_aspect_ratio_policy="not_larger"),
+    dict(x=(1, 1, 2, 2), sizes=[7, 8], axes=[2, 3], keep_aspect_ratio_policy="not_smaller"),
+    dict(x=(1, 1, 2, 4), sizes=[1, 3], axes=[2, 3], keep_aspect_ratio_policy="not_smaller"),
+    dict(x=(1, 1, 4, 4), sizes=[3, 3], axes=[3, 2], roi=[0.6, 0.4, 0.8, 0.6],
+         coordinate_transformation_mode="tf_crop_and_resize"),
+    dict(x=(1, 1, 4, 4), scales=[0.8, 0.5], axes=[-1, -2], roi=[0.2, 0.0, 0.9, 1.0],
+         coordinate_transformation_mode="tf_crop_and_resize"),
+    dict(x=(5, 9, 3), scales=[1, 2.5, 1 / 3]),
+])
+def test_resize_output_shape_matches_oracle(L, oracle_mod, case):
+    case = dict(case)
+    x = case.pop("x")
+    got = _resize_shape_lib(x, **case)
+    coord = case.get("coordinate_transformation_mode", "half_pixel")
+    keep = case.get("keep_aspect_ratio_policy", "stretch")
+    exp = oracle_mod.resize_shape(x, case.get("scales"), case.get("sizes"), case.get("roi"),
+                                  case.get("axes"), coord, keep)[0]
+    assert got == exp
+
+
+def test_resize_rejects_bad_arguments_on_the_host(L):
+    at = gs.resize_attrs()
+    f32 = lambda *v: (ctypes.c_float * len(v))(*v)
+    shape = _i64([1, 1, 4, 4])
+    out = (ctypes.c_int64 * 4)()
+    # both scales and sizes, neither, a zero scale, a repeated axis, a bad mode
+    assert L.gs_resize_output_shape(4, shape, None, 0, f32(1, 1, 2, 2), _i64([1, 1, 8, 8]), None,
+                                    ctypes.byref(at), out) == 5
+    assert L.gs_resize_output_shape(4, shape, None, 0, None, None, None, ctypes.byref(at), out) == 5
+    assert L.gs_resize_output_shape(4, shape, None, 0, f32(1, 1, 0, 2), None, None,
+                                    ctypes.byref(at), out) == 5
+    assert L.gs_resize_output_shape(4, shape, _i64([2, -2]), 2, f32(2, 2), None, None,
+                                    ctypes.byref(at), out) == 3
+    bad = gs.resize_attrs()
+    bad.mode = 7
+    assert L.gs_resize_output_shape(4, shape, None, 0, f32(1, 1, 2, 2), None, None,
+                                    ctypes.byref(bad), out) == 5
+    # four resized axes, and an antialiased downscale needing more than 64 taps
+    four = _i64([2, 2, 4, 4])
+    assert L.gs_resize(FAKE, 4, four, None, 0, f32(2, 1, 2, 2), None, None, ctypes.byref(at), 0,
+                       FAKE, None) == 9
+    aa = gs.resize_attrs(mode="cubic", antialias=1)
+    big = _i64([1, 1, 1024, 1024])
+    assert L.gs_resize(FAKE, 4, big, None, 0, f32(1, 1, 0.01, 0.01), None, None, ctypes.byref(aa),
+                       0, FAKE, None) == 9
+    # an empty output needs no pointers; an empty input with a nonempty output is a shape error
+    assert L.gs_resize(None, 4, _i64([1, 1, 4, 4]), None, 0, None, _i64([1, 1, 0, 3]), None,
+                       ctypes.byref(at), 0, None, None) == 0
+    assert L.gs_resize(FAKE, 4, _i64([1, 1, 0, 4]), None, 0, None, _i64([1, 1, 3, 3]), None,
+                       ctypes.byref(at), 0, FAKE, None) == 3
