@@ -138,6 +138,30 @@ gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const 
                             int align_corners, float cubic_coeff_a, void *workspace,
                             size_t workspace_bytes, void *Y, cudaStream_t stream);
 
+/* Integer element types of X for gs_grid_sample_int. */
+typedef enum { GS_U8 = 16, GS_I8 = 17, GS_U16 = 18, GS_I16 = 19 } gs_itype;
+
+/*
+ * gs_grid_sample_int -- GridSample - version 20 with an integer-typed X
+ * (Type Constraints, T1; Outputs: "for integer input types, intermediate
+ * values are computed as floating point and cast to integer at the end").
+ *
+ *   X, Y     device, integer type `xt` (uint8, int8, uint16, int16), the
+ *            layouts of gs_grid_sample.
+ *   grid     device, floating type `grid_dt` (T2: float, float16; bfloat16
+ *            as in version 22).
+ *   Other arguments, and the taps and weights, as gs_grid_sample.
+ *
+ * X is widened to fp32 (exact for these types), interpolated in fp32, then
+ * truncated toward zero and saturated at the range of `xt` (cubic weights can
+ * overshoot it).  Errors as gs_grid_sample; GS_ERR_DTYPE for another `xt` or
+ * `grid_dt`.
+ */
+gs_status gs_grid_sample_int(const void *X, gs_itype xt, const int64_t *x_shape, int r,
+                             const void *grid, gs_dtype grid_dt, const int64_t *out_spatial,
+                             gs_mode mode, gs_pad pad, int align_corners, float cubic_coeff_a,
+                             void *Y, cudaStream_t stream);
+
 /* Size of the scratch gs_grid_sample_static uses: 64 MiB per device. */
 #define GS_STATIC_WORKSPACE_BYTES (64u << 20)
 

@@ -311,3 +311,15 @@ def resize(X, scales=None, sizes=None, roi=None, axes=None, mode="nearest",
                            int(exclude_outside), float(extrapolation_value), int(antialias),
                            _p(Y)))
     return Y
+
+
+INT_RANGES = {"uint8": (0, 255), "int8": (-128, 127), "uint16": (0, 65535), "int16": (-32768, 32767)}
+
+
+def cast_to_integer(values, dtype):
+    """GridSample - version 20, Outputs: integer X is interpolated in floating point and
+    cast to the integer type at the end.  Reading: truncation toward zero, saturated at
+    the type's range (cubic weights can overshoot it)."""
+    lo, hi = INT_RANGES[dtype]
+    v = np.clip(np.asarray(values, dtype=np.float64), lo, hi)
+    return np.trunc(v).astype(np.int64)

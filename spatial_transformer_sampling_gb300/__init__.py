@@ -30,7 +30,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libgs.so")
 
 EXPORTED_SYMBOLS = ("gs_affine_grid", "gs_grid_sample", "gs_affine_sample", "gs_deform_conv",
-                    "gs_resize", "gs_resize_output_shape", "gs_status_str", "gs_device_status",
+                    "gs_resize", "gs_resize_output_shape", "gs_grid_sample_int", "gs_status_str",
+                    "gs_device_status",
                     "gs_version")
 
 MODES = {"linear": 0, "bilinear": 0, "nearest": 1, "cubic": 2, "bicubic": 2}
@@ -96,6 +97,7 @@ def load_library(path=None):
                                                 ci, ctypes.POINTER(ctypes.c_size_t)]
     L.gs_deform_conv_ws.argtypes = [vp, i64p, vp, ctypes.c_int64, vp, vp, vp,
                                     ctypes.POINTER(DeformAttrs), ci, vp, ctypes.c_size_t, vp, vp]
+    L.gs_grid_sample_int.argtypes = [vp, ci, i64p, ci, vp, ci, i64p, ci, ci, ci, cf, vp, vp]
     f32p = ctypes.POINTER(ctypes.c_float)
     L.gs_resize_output_shape.argtypes = [ci, i64p, i64p, ci, f32p, i64p, f32p,
                                          ctypes.POINTER(ResizeAttrs), i64p]
@@ -108,7 +110,7 @@ def load_library(path=None):
     for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
               "gs_grid_sample_ws", "gs_grid_sample_static", "gs_affine_sample", "gs_deform_conv",
               "gs_deform_conv_workspace_size", "gs_deform_conv_ws", "gs_device_status",
-              "gs_resize_output_shape", "gs_resize"):
+              "gs_resize_output_shape", "gs_resize", "gs_grid_sample_int"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -198,6 +200,36 @@ def gs_grid_sample(X, grid, mode="linear", padding_mode="zeros", align_corners=0
                                       _dtype_code(X), MODES[mode], PADS[padding_mode],
                                       int(align_corners), float(cubic_coeff_a), _ptr(out),
                                       _stream(X)), "gs_grid_sample")
+    return out
+
+
+def _int_code(t):
+    torch = _torch()
+    codes = {torch.uint8: 16, torch.int8: 17, torch.int16: 19}
+    if hasattr(torch, "uint16"):
+        codes[torch.uint16] = 18
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported integer dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def gs_grid_sample_int(X, grid, mode="linear", padding_mode="zeros", align_corners=0,
+                       cubic_coeff_a=-0.75, out=None):
+    """GridSample with an integer X (uint8, int8, uint16, int16) and a float grid: fp32
+    intermediates, truncated toward zero and saturated at the end (gs_grid_sample_int)."""
+    torch = _torch()
+    for t in (X, grid, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("libgs takes contiguous CUDA tensors")
+    r = X.dim() - 2
+    out_sp = list(grid.shape[1:-1])
+    if out is None:
+        out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
+    _ok(load_library().gs_grid_sample_int(_ptr(X), _int_code(X), _i64(X.shape), r, _ptr(grid),
+                                          _dtype_code(grid), _i64(out_sp), MODES[mode],
+                                          PADS[padding_mode], int(align_corners),
+                                          float(cubic_coeff_a), _ptr(out), _stream(X)),
+        "gs_grid_sample_int")
     return out
 
 

@@ -415,6 +415,39 @@ gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const voi
     });
 }
 
+gs_status gs_grid_sample_int(const void *X, gs_itype xt, const int64_t *x_shape, int r,
+                             const void *grid, gs_dtype grid_dt, const int64_t *out_spatial,
+                             gs_mode mode, gs_pad pad, int align_corners, float cubic_coeff_a,
+                             void *Y, cudaStream_t stream) {
+    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (xt != GS_U8 && xt != GS_I8 && xt != GS_U16 && xt != GS_I16) return GS_ERR_DTYPE;
+    gs::SampleArgs args;
+    bool skip = false;
+    // shape and attribute checks as gs_grid_sample, with the grid's float type
+    gs_status st = check_sample_shape(x_shape, r, out_spatial, grid_dt, mode, pad, align_corners,
+                                      cubic_coeff_a, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    const size_t xs = (xt == GS_U8 || xt == GS_I8) ? 1 : 2;
+    if (!X || !Y || !grid) return GS_ERR_NULL;
+    if (!aligned(X, xs) || !aligned(Y, xs) || !aligned(grid, elem_size(grid_dt))) return GS_ERR_ALIGN;
+    cudaError_t e;
+    switch (xt) {
+        case GS_U8:
+            e = gs::launch_sample_int<uint8_t>(X, grid, (int)grid_dt, Y, args, r, (int)mode, stream);
+            break;
+        case GS_I8:
+            e = gs::launch_sample_int<int8_t>(X, grid, (int)grid_dt, Y, args, r, (int)mode, stream);
+            break;
+        case GS_U16:
+            e = gs::launch_sample_int<uint16_t>(X, grid, (int)grid_dt, Y, args, r, (int)mode, stream);
+            break;
+        default:
+            e = gs::launch_sample_int<int16_t>(X, grid, (int)grid_dt, Y, args, r, (int)mode, stream);
+            break;
+    }
+    return e == cudaSuccess ? GS_OK : GS_ERR_CUDA;
+}
+
 gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int64_t *out_spatial,
                                         gs_dtype dt, size_t *bytes) {
     if (!bytes) return GS_ERR_NULL;

@@ -54,6 +54,22 @@ template <> struct IO<__nv_bfloat16> {
     static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
+// Integer X (GridSample - version 20, Outputs: for integer input types the
+// intermediate values are floating point, cast to the integer type at the
+// end).  The cast truncates toward zero and saturates at the type's range
+// (cubic weights can overshoot it); NaN reads as 0.
+template <typename I, int LO, int HI> struct IntIO {
+    static __device__ __forceinline__ float ld(const I *p) { return (float)__ldg(p); }
+    static __device__ __forceinline__ I st(float v) {
+        v = fminf(fmaxf(v, (float)LO), (float)HI);   // fmaxf(NaN, LO) is LO
+        return (I)(int)v;                             // truncation toward zero
+    }
+};
+template <> struct IO<uint8_t> : IntIO<uint8_t, 0, 255> {};
+template <> struct IO<int8_t> : IntIO<int8_t, -128, 127> {};
+template <> struct IO<uint16_t> : IntIO<uint16_t, 0, 65535> {};
+template <> struct IO<int16_t> : IntIO<int16_t, -32768, 32767> {};
+
 // ------------------------------------------------------------- axis params
 
 // One input spatial axis, precomputed on the host.

@@ -99,5 +99,10 @@ template <typename T>
 size_t deform_ws_bytes(const DeformArgs &args);
 template <typename T>
 cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &args, cudaStream_t s);
+// GridSample with integer X (TX: uint8_t, int8_t, uint16_t, int16_t) and a float
+// grid of gs_dtype code `grid_dt`.
+template <typename TX>
+cudaError_t launch_sample_int(const void *X, const void *grid, int grid_dt, void *Y,
+                              const SampleArgs &args, int r, int mode, cudaStream_t s);
 
 }  // namespace gs

@@ -208,3 +208,16 @@ def test_resize_rejects_bad_arguments_on_the_host(L):
                        ctypes.byref(at), 0, None, None) == 0
     assert L.gs_resize(FAKE, 4, _i64([1, 1, 0, 4]), None, 0, None, _i64([1, 1, 3, 3]), None,
                        ctypes.byref(at), 0, FAKE, None) == 3
+
+
+def test_integer_x_entry_rejects_bad_types_on_the_host(L):
+    xs, out = _i64([1, 2, 4, 4]), _i64([3, 3])
+    # X type not an integer code, grid type not a float code, bad rank
+    assert L.gs_grid_sample_int(FAKE, 0, xs, 2, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 4
+    assert L.gs_grid_sample_int(FAKE, 16, xs, 2, FAKE, 9, out, 0, 0, 0, -0.75, FAKE, None) == 4
+    assert L.gs_grid_sample_int(FAKE, 16, xs, 4, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 2
+    # misaligned int16 X
+    assert L.gs_grid_sample_int(FAKE + 1, 19, xs, 2, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 6
+    # empty output: no launch, no pointers needed
+    assert L.gs_grid_sample_int(None, 16, xs, 2, None, 0, _i64([0, 3]), 0, 0, 0, -0.75, None,
+                                None) == 0

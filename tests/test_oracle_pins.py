@@ -456,3 +456,13 @@ def test_deform_point_evaluator_matches_full_output(oracle_mod):
                                      dilations=case["dil"], group=case["group"],
                                      offset_group=case["og"])
     np.testing.assert_array_equal(vals, Y.ravel()[idx])
+
+
+def test_integer_cast_truncates_toward_zero_and_saturates(oracle_mod):
+    v = np.array([-129.7, -128.0, -2.9, -0.4, 0.0, 0.99, 3.0, 126.999, 127.5, 300.0])
+    np.testing.assert_array_equal(oracle_mod.cast_to_integer(v, "int8"),
+                                  [-128, -128, -2, 0, 0, 0, 3, 126, 127, 127])
+    np.testing.assert_array_equal(oracle_mod.cast_to_integer(v, "uint8"),
+                                  [0, 0, 0, 0, 0, 0, 3, 126, 127, 255])
+    np.testing.assert_array_equal(oracle_mod.cast_to_integer([70000.2, -5.0], "uint16"), [65535, 0])
+    np.testing.assert_array_equal(oracle_mod.cast_to_integer([-40000.0, 1.5], "int16"), [-32768, 1])
