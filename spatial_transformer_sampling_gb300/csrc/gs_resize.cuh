@@ -37,18 +37,38 @@ struct ResizeTile {
     int tiles[3];    // tiles along each axis
 };
 
-__device__ __forceinline__ double rs_keys(double s, double a) {
+__host__ __device__ inline double rs_keys(double s, double a) {
     s = fabs(s);
     if (s <= 1.0) return ((a + 2.0) * s - (a + 3.0)) * s * s + 1.0;
     if (s < 2.0) return ((a * s - 5.0 * a) * s + 8.0 * a) * s - 4.0 * a;
     return 0.0;
 }
 
+// Products and sums that decide a tap index or the crop test are rounded one
+// by one (no fused multiply-add), on the host and the device alike.
+__host__ __device__ inline double rs_mul(double a, double b) {
+#ifdef __CUDA_ARCH__
+    return __dmul_rn(a, b);
+#else
+    return a * b;
+#endif
+}
+__host__ __device__ inline double rs_add(double a, double b) {
+#ifdef __CUDA_ARCH__
+    return __dadd_rn(a, b);
+#else
+    return a + b;
+#endif
+}
+
 // Taps of output index o on axis A: indices clamped to the axis (edge values),
 // weights; returns the count, or -1 when the element takes
 // extrapolation_value.  The count depends only on the axis (the host sets it
-// with A.k0 and A.taps), so every entry of a table has the same length.
-static __device__ int rs_axis_taps(int o, const ResizeAxis &A, const ResizeArgs &p, int *idx, float *w) {
+// with A.k0 and A.taps), so every entry of a table has the same length.  Runs
+// on the host (tables passed to resize_rows_kernel) and on the device (tables
+// built per block by resize_kernel).
+__host__ __device__ inline int rs_axis_taps(int o, const ResizeAxis &A, const ResizeArgs &p,
+                                            int *idx, float *w) {
     const double xr = (double)o;
     double x;
     switch (p.coord) {
@@ -56,16 +76,18 @@ static __device__ int rs_axis_taps(int o, const ResizeAxis &A, const ResizeArgs 
             x = A.n_out > 1 ? (xr + 0.5) / A.scale - 0.5 : 0.0;
             break;
         case RS_ALIGN_CORNERS:
-            x = A.length_resized > 1.0 ? xr * (double)(A.n_in - 1) / (A.length_resized - 1.0) : 0.0;
+            x = A.length_resized > 1.0 ? rs_mul(xr, (double)(A.n_in - 1)) / (A.length_resized - 1.0)
+                                       : 0.0;
             break;
         case RS_ASYMMETRIC:
             x = xr / A.scale;
             break;
         case RS_TF_CROP_AND_RESIZE:
-            x = A.n_out > 1 ? A.roi_start * (double)(A.n_in - 1) +
-                                  xr * (A.roi_end - A.roi_start) * (double)(A.n_in - 1) /
-                                      (double)(A.n_out - 1)
-                            : 0.5 * (A.roi_start + A.roi_end) * (double)(A.n_in - 1);
+            x = A.n_out > 1
+                    ? rs_add(rs_mul(A.roi_start, (double)(A.n_in - 1)),
+                             rs_mul(rs_mul(xr, A.roi_end - A.roi_start), (double)(A.n_in - 1)) /
+                                 (double)(A.n_out - 1))
+                    : rs_mul(rs_mul(0.5, A.roi_start + A.roi_end), (double)(A.n_in - 1));
             break;
         default:   // half_pixel
             x = (xr + 0.5) / A.scale - 0.5;
@@ -320,6 +342,206 @@ resize_kernel(const T *__restrict__ X, T *__restrict__ Y, const ResizeArgs p, co
     }
 }
 
+// ------------------------------------------------------------------
+// Row kernel (resizes of one or two trailing axes): per-axis tap tables built
+// once on the host, in the same fp64 arithmetic, and passed as a kernel
+// parameter.  A block owns a band of output rows, full width, for a range of
+// slices; a thread owns output columns x = tid, tid + 256, ... (at most four)
+// and keeps their taps in registers.  Warps read whole input rows.
+
+constexpr int kRsTableBytes = 30 * 1024;   // kernel parameters hold up to 32 KB
+constexpr int kRsRowsMaxCols = 4;           // output columns per thread
+
+struct ResizeTables {
+    int nx, ny, kx, ky;   // output extents (rows axis, columns axis) and taps per index
+    // x idx[nx*kx] (int), x w[nx*kx] (float), y idx[ny*ky], y w[ny*ky],
+    // x flags[nx], y flags[ny] (1: extrapolation_value)
+    unsigned char data[kRsTableBytes];
+};
+
+inline size_t rs_table_bytes(int nx, int kx, int ny, int ky) {
+    return ((size_t)nx * kx + (size_t)ny * ky) * 8 + (size_t)nx + (size_t)ny;
+}
+
+template <typename T, int KY, int KX>
+__global__ void __launch_bounds__(kRsThreads)
+resize_rows_kernel(const T *__restrict__ X, T *__restrict__ Y, const __grid_constant__ ResizeTables tb,
+                   int64_t B, int H, int W, int rows_per_block, int slices_per_block,
+                   float extrapolation_value) {
+    const int nx = tb.nx, ny = tb.ny;
+    const int *xi = reinterpret_cast<const int *>(tb.data);
+    const float *xw = reinterpret_cast<const float *>(tb.data + (size_t)nx * KX * 4);
+    const int *yi = reinterpret_cast<const int *>(tb.data + (size_t)nx * KX * 8);
+    const float *yw = reinterpret_cast<const float *>(tb.data + (size_t)nx * KX * 8 + (size_t)ny * KY * 4);
+    const unsigned char *xf = tb.data + ((size_t)nx * KX + (size_t)ny * KY) * 8;
+    const unsigned char *yf = xf + nx;
+
+    const int y0 = blockIdx.x * rows_per_block;
+    const int y1 = min(ny, y0 + rows_per_block);
+    const int64_t b0 = (int64_t)blockIdx.y * slices_per_block;
+    const int64_t b1 = min(B, b0 + slices_per_block);
+    const int tid = threadIdx.x;
+
+    // this thread's columns and their taps
+    int cx[kRsRowsMaxCols][KX];
+    float cw[kRsRowsMaxCols][KX];
+    bool cf[kRsRowsMaxCols];
+    int ncols = 0;
+#pragma unroll
+    for (int j = 0; j < kRsRowsMaxCols; ++j) {
+        const int x = tid + j * kRsThreads;
+        const bool in = x < nx;
+        if (in) ncols = j + 1;
+#pragma unroll
+        for (int k = 0; k < KX; ++k) {
+            cx[j][k] = in ? xi[x * KX + k] : 0;
+            cw[j][k] = in ? xw[x * KX + k] : 0.0f;
+        }
+        cf[j] = in && xf[x];
+    }
+    const int64_t in_slice = (int64_t)H * W, out_slice = (int64_t)ny * nx;
+    // rows outer (their taps read once), slices inner, four slices per step so
+    // their loads are in flight together
+    for (int y = y0; y < y1; ++y) {
+        int ry[KY];
+        float wy[KY];
+#pragma unroll
+        for (int k = 0; k < KY; ++k) {
+            ry[k] = yi[y * KY + k];
+            wy[k] = yw[y * KY + k];
+        }
+        const bool fy = yf[y] != 0;
+#pragma unroll
+        for (int j = 0; j < kRsRowsMaxCols; ++j) {
+            if (j >= ncols) break;
+            const int x = tid + j * kRsThreads;
+            const T *rows[KY];
+#pragma unroll
+            for (int k = 0; k < KY; ++k) rows[k] = X + b0 * in_slice + (int64_t)ry[k] * W;
+            T *yp = Y + b0 * out_slice + (int64_t)y * nx + x;
+            if (fy || cf[j]) {
+                const T v = IO<T>::st(extrapolation_value);
+                for (int64_t b = b0; b < b1; ++b, yp += out_slice) *yp = v;
+                continue;
+            }
+            int64_t b = b0;
+            for (; b + 4 <= b1; b += 4) {
+                float acc[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc[u] = 0.0f;
+#pragma unroll
+                    for (int ky = 0; ky < KY; ++ky) {
+                        const T *row = rows[ky] + u * in_slice;
+                        float sx = 0.0f;
+#pragma unroll
+                        for (int kx = 0; kx < KX; ++kx) sx = fmaf(cw[j][kx], IO<T>::ld(row + cx[j][kx]), sx);
+                        acc[u] = fmaf(wy[ky], sx, acc[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) yp[u * out_slice] = IO<T>::st(acc[u]);
+#pragma unroll
+                for (int k = 0; k < KY; ++k) rows[k] += 4 * in_slice;
+                yp += 4 * out_slice;
+            }
+            for (; b < b1; ++b) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int ky = 0; ky < KY; ++ky) {
+                    float sx = 0.0f;
+#pragma unroll
+                    for (int kx = 0; kx < KX; ++kx) sx = fmaf(cw[j][kx], IO<T>::ld(rows[ky] + cx[j][kx]), sx);
+                    acc = fmaf(wy[ky], sx, acc);
+                }
+                *yp = IO<T>::st(acc);
+#pragma unroll
+                for (int k = 0; k < KY; ++k) rows[k] += in_slice;
+                yp += out_slice;
+            }
+        }
+    }
+}
+
+// Row kernel for r <= 2 and fixed tap counts when the tables fit the kernel
+// parameters; *used reports whether it ran.
+template <typename T>
+cudaError_t launch_resize_rows(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s,
+                               bool *used) {
+    *used = false;
+    if (p.r > 2) return cudaSuccess;
+    const ResizeAxis &AX = p.ax[2], &AY = p.ax[1];
+    const int kx = AX.taps, ky = p.r == 2 ? AY.taps : 1;
+    const bool ok_taps = (p.r == 2 && kx == ky && (kx == 1 || kx == 2 || kx == 4)) ||
+                         (p.r == 1 && (kx == 1 || kx == 2 || kx == 4));
+    if (!ok_taps || AX.n_out > kRsThreads * kRsRowsMaxCols) return cudaSuccess;
+    const int nx = AX.n_out, ny = p.r == 2 ? AY.n_out : 1;
+    if (rs_table_bytes(nx, kx, ny, ky) > (size_t)kRsTableBytes) return cudaSuccess;
+    ResizeTables tb;
+    tb.nx = nx;
+    tb.ny = ny;
+    tb.kx = kx;
+    tb.ky = ky;
+    int *xi = reinterpret_cast<int *>(tb.data);
+    float *xw = reinterpret_cast<float *>(tb.data + (size_t)nx * kx * 4);
+    int *yi = reinterpret_cast<int *>(tb.data + (size_t)nx * kx * 8);
+    float *yw = reinterpret_cast<float *>(tb.data + (size_t)nx * kx * 8 + (size_t)ny * ky * 4);
+    unsigned char *xf = tb.data + ((size_t)nx * kx + (size_t)ny * ky) * 8;
+    unsigned char *yf = xf + nx;
+    int ib[kRsMaxTaps];
+    float wb[kRsMaxTaps];
+    for (int o = 0; o < nx; ++o) {
+        const int c = rs_axis_taps(o, AX, p, ib, wb);
+        xf[o] = c < 0 ? 1 : 0;
+        for (int k = 0; k < kx; ++k) {
+            xi[o * kx + k] = c < 0 ? 0 : ib[k];
+            xw[o * kx + k] = c < 0 ? 0.0f : wb[k];
+        }
+    }
+    for (int o = 0; o < ny; ++o) {
+        int c = 1;
+        if (p.r == 2) {
+            c = rs_axis_taps(o, AY, p, ib, wb);
+        } else {
+            ib[0] = 0;
+            wb[0] = 1.0f;
+        }
+        yf[o] = c < 0 ? 1 : 0;
+        for (int k = 0; k < ky; ++k) {
+            yi[o * ky + k] = c < 0 ? 0 : ib[k];
+            yw[o * ky + k] = c < 0 ? 0.0f : wb[k];
+        }
+    }
+    // enough blocks for several waves: bands of rows x chunks of slices
+    int rows = 8;
+    int64_t per = 64;
+    auto blocks = [&](int r_, int64_t p_) {
+        return (int64_t)((ny + r_ - 1) / r_) * ((p.B + p_ - 1) / p_);
+    };
+    while (per > 1 && blocks(rows, per) < 8 * 152) per >>= 1;
+    while (rows > 1 && blocks(rows, per) < 8 * 152) rows >>= 1;
+    per = std::max<int64_t>(per, (p.B + 65534) / 65535);
+    const dim3 grid((unsigned)((ny + rows - 1) / rows), (unsigned)((p.B + per - 1) / per));
+    const int H = p.r == 2 ? AY.n_in : 1, W = AX.n_in;
+    if (kx == 1 && ky == 1)
+        resize_rows_kernel<T, 1, 1><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
+                                                                rows, (int)per, p.extrapolation_value);
+    else if (ky == 1 && kx == 2)
+        resize_rows_kernel<T, 1, 2><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
+                                                                rows, (int)per, p.extrapolation_value);
+    else if (ky == 1 && kx == 4)
+        resize_rows_kernel<T, 1, 4><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
+                                                                rows, (int)per, p.extrapolation_value);
+    else if (kx == 2)
+        resize_rows_kernel<T, 2, 2><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
+                                                                rows, (int)per, p.extrapolation_value);
+    else
+        resize_rows_kernel<T, 4, 4><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
+                                                                rows, (int)per, p.extrapolation_value);
+    *used = true;
+    return cudaGetLastError();
+}
+
 template <typename T, int R>
 static cudaError_t launch_resize_r(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s) {
     // tile: up to 256 positions, innermost axis widest
@@ -360,6 +582,9 @@ static cudaError_t launch_resize_r(const void *X, void *Y, const ResizeArgs &p, 
 
 template <typename T>
 cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s) {
+    bool used = false;
+    const cudaError_t e = launch_resize_rows<T>(X, Y, p, s, &used);
+    if (used || e != cudaSuccess) return e;
     if (p.r == 1) return launch_resize_r<T, 1>(X, Y, p, s);
     if (p.r == 2) return launch_resize_r<T, 2>(X, Y, p, s);
     return launch_resize_r<T, 3>(X, Y, p, s);
