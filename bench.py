@@ -244,7 +244,7 @@ class Case:
                 nbytes = gs.gs_deform_conv_workspace_size(w.x_shape, w.oc, a, getattr(torch, dtype))
                 if nbytes:
                     self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-                    self.launches = 3   # pack W, copy X, sample + contract
+                    self.launches = 2   # pack W with copy X, then sample + contract
                     self.kernel_tag = f"deform_tc_nhwc<{DT_SHORT[dtype]}>"
         self.dev = {k: v.to(device) for k, v in self.host.items()}
         self.out = torch.empty(self._out_shape(), dtype=self.dev["X"].dtype, device=device)

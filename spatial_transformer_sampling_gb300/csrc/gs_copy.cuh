@@ -27,13 +27,11 @@ template <typename T> using RawOf = typename std::conditional<sizeof(T) == 4, ui
 // (ct, pt, n) = blockIdx.x; blocks with pt = 0 also zero their channels of the
 // slot's zero pixel.  Elements move as raw bits.
 template <typename R, int TC>
-__global__ void __launch_bounds__(256)
-nchw_to_nhwc_kernel(const R *__restrict__ X, R *__restrict__ ws, int C, int64_t P, int ctiles,
-                    int64_t ptiles) {
+__device__ __forceinline__ void nchw_to_nhwc_block(const R *__restrict__ X, R *__restrict__ ws,
+                                                   int C, int64_t P, int ctiles, int64_t ptiles,
+                                                   int64_t b, R (&tile)[TC][4096 / TC + 1]) {
     constexpr int TP = 4096 / TC;               // pixels per tile
     constexpr int E = 16 / (int)sizeof(R);      // elements per 16-byte vector
-    __shared__ R tile[TC][TP + 1];
-    int64_t b = blockIdx.x;
     const int ct = (int)(b % ctiles);
     b /= ctiles;
     const int64_t pt = b % ptiles;
@@ -90,6 +88,14 @@ nchw_to_nhwc_kernel(const R *__restrict__ X, R *__restrict__ ws, int C, int64_t 
         memcpy(&u, v, 16);
         *reinterpret_cast<uint4 *>(dst + gp * C + gc) = u;
     }
+}
+
+template <typename R, int TC>
+__global__ void __launch_bounds__(256)
+nchw_to_nhwc_kernel(const R *__restrict__ X, R *__restrict__ ws, int C, int64_t P, int ctiles,
+                    int64_t ptiles) {
+    __shared__ R tile[TC][4096 / TC + 1];
+    nchw_to_nhwc_block<R, TC>(X, ws, C, P, ctiles, ptiles, (int64_t)blockIdx.x, tile);
 }
 
 // Copy tiles per image for C channels and P positions: TC channels (the

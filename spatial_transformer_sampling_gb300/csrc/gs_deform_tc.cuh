@@ -285,11 +285,10 @@ cudaError_t launch_deform_tc(const void *X, const void *W, const void *offset, c
 
 // W[oc, c, k] -> workspace, K-major core-matrix rows of 8 channels (16 bytes)
 // per (k, oc): byte k * oC*C*2 + (oc / 8) * C*16 + (c / 8) * 128 + (oc % 8) * 16.
+// Element e of the pack (one 16-byte row); e < K * oC * (C / 8).
 template <typename T>
-__global__ void __launch_bounds__(256)
-deform_pack_w_kernel(const T *__restrict__ Wt, uint16_t *__restrict__ wp, int oC, int C, int K) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= K * oC * (C / 8)) return;
+__device__ __forceinline__ void deform_pack_w_row(const T *__restrict__ Wt, uint16_t *__restrict__ wp,
+                                                  int oC, int C, int K, int e) {
     const int c8 = e % (C / 8);
     const int oc = (e / (C / 8)) % oC;
     const int k = e / ((C / 8) * oC);
@@ -301,6 +300,23 @@ deform_pack_w_kernel(const T *__restrict__ Wt, uint16_t *__restrict__ wp, int oC
     memcpy(&u, v, 16);
     *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(wp) + (size_t)k * oC * C * 2 +
                                (size_t)(oc / 8) * C * 16 + c8 * 128 + (oc % 8) * 16) = u;
+}
+
+// One launch for the channel-last path's preparation: blocks below
+// copy_blocks copy X to the slots (nchw_to_nhwc_block), the rest pack W.
+template <typename T, int TC>
+__global__ void __launch_bounds__(256)
+deform_prep_kernel(const uint16_t *__restrict__ X, uint16_t *__restrict__ slots, int C, int64_t P,
+                   int ctiles, int64_t ptiles, int64_t copy_blocks, const T *__restrict__ Wt,
+                   uint16_t *__restrict__ wp, int oC, int K) {
+    __shared__ uint16_t tile[TC][4096 / TC + 1];
+    const int64_t b = blockIdx.x;
+    if (b < copy_blocks) {
+        nchw_to_nhwc_block<uint16_t, TC>(X, slots, C, P, ctiles, ptiles, b, tile);
+        return;
+    }
+    const int e = (int)(b - copy_blocks) * blockDim.x + threadIdx.x;
+    if (e < K * oC * (C / 8)) deform_pack_w_row<T>(Wt, wp, oC, C, K, e);
 }
 
 // Offsets and mask of position p's kernel tap k (plane = P positions).
@@ -610,8 +626,6 @@ cudaError_t launch_deform_tc_ws(const void *X, const void *W, const void *offset
     }
     const int K = a.kH * a.kW;
     const int packs = K * a.oC * (a.C / 8);
-    deform_pack_w_kernel<T><<<(unsigned)((packs + 255) / 256), 256, 0, s>>>(
-        (const T *)W, (uint16_t *)ws, a.oC, a.C, K);
     uint16_t *slots = (uint16_t *)((unsigned char *)ws + wreg);
     const int64_t HW = (int64_t)a.H * a.W;
     const int64_t max_blocks = ((int64_t)1 << 31) - 1;
@@ -620,7 +634,30 @@ cudaError_t launch_deform_tc_ws(const void *X, const void *W, const void *offset
     per = std::min<int64_t>(per, std::max<int64_t>(1, max_blocks / q.tiles));
     for (int64_t n0 = 0; n0 < a.N; n0 += per) {
         const int64_t nc = std::min<int64_t>(per, a.N - n0);
-        launch_copy_to_slots<uint16_t>((const uint16_t *)X + n0 * a.C * HW, slots, nc, a.C, HW, s);
+        if (n0 == 0) {
+            // the first chunk's copy and the W pack share one launch
+            const int TC = copy_tc(a.C);
+            const int ctiles = (a.C + TC - 1) / TC;
+            const int64_t ptiles = (HW + 4096 / TC - 1) / (4096 / TC);
+            const int64_t copy_blocks = nc * ctiles * ptiles;
+            const unsigned blocks = (unsigned)(copy_blocks + (packs + 255) / 256);
+            const uint16_t *Xc = (const uint16_t *)X;
+            if (TC == 16)
+                deform_prep_kernel<T, 16><<<blocks, 256, 0, s>>>(Xc, slots, a.C, HW, ctiles, ptiles,
+                                                                copy_blocks, (const T *)W,
+                                                                (uint16_t *)ws, a.oC, K);
+            else if (TC == 32)
+                deform_prep_kernel<T, 32><<<blocks, 256, 0, s>>>(Xc, slots, a.C, HW, ctiles, ptiles,
+                                                                copy_blocks, (const T *)W,
+                                                                (uint16_t *)ws, a.oC, K);
+            else
+                deform_prep_kernel<T, 64><<<blocks, 256, 0, s>>>(Xc, slots, a.C, HW, ctiles, ptiles,
+                                                                copy_blocks, (const T *)W,
+                                                                (uint16_t *)ws, a.oC, K);
+        } else {
+            launch_copy_to_slots<uint16_t>((const uint16_t *)X + n0 * a.C * HW, slots, nc, a.C, HW,
+                                           s);
+        }
         const unsigned blocks = (unsigned)(nc * q.tiles);
         const T *Xs = (const T *)slots;
         if (q.kc == 64)
