@@ -111,19 +111,6 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
     }
 }
 
-// Arrives once on `bar` when every cp.async this thread issued so far has
-// completed (the arrival counts toward the barrier's expected count).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-// Plain arrive (release semantics: this thread's earlier shared-memory reads
-// and writes are ordered before it).
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Packed fp32 pairs (Blackwell): lane-wise a*b and a*b+c, each rounded to
 // nearest exactly as fmulf / fmaf would round it.
 __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
