@@ -15,8 +15,12 @@ taken with CUDA events on the stream the kernel runs on; the timed region is
 bracketed by barrier + synchronize, and the max over ranks is reported.
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
-(the images are independent; there is no exchange step) and `value` is the
-whole job's output elements per second.
+(the images are independent; there is no exchange step; rank r draws its
+images at the workload's seed + r) and `value` is the whole job's output
+elements per second over the slowest rank's time.
+
+Beside the cold-L2 headline the line carries the median step time and a
+warm-L2 figure (the same steps back to back, no flush).
 
 --impl reference times the CPU oracle (plain C, fp64, OpenMP over output
 elements) on a bounded sample of the same workload and prints the same JSON
@@ -60,6 +64,8 @@ def parse():
     p.add_argument("--workspace", action="store_true",
                    help="GridSample workloads: gs_grid_sample_ws with the workspace it asks for")
     p.add_argument("--extra-steps", type=int, default=100)
+    p.add_argument("--sample-seconds", type=float, default=20.0,
+                   help="--impl reference: oracle time per step (a bounded sample of the batch)")
     return p.parse_args()
 
 
@@ -121,6 +127,42 @@ def recorded_traffic(kernel_tag, workload, dtype):
                 and kv.get("dtype") == dtype and kv.get("src_sha") == sha):
             return float(kv["dram_bytes_per_launch"])
     return None
+
+
+def host_inputs(w, dtype, seed):
+    """One replica's seeded inputs on the host, rounded to dtype (torch CPU tensors)."""
+    if w.kind == "affine_sample":
+        inp = wl.make_affine_sample_inputs(w, seed=seed)
+        return {"theta": wl.as_dtype(inp["theta"], dtype), "X": wl.as_dtype(inp["X"], dtype)}
+    if w.kind == "grid_sample":
+        inp = wl.make_grid_sample_inputs(w, seed=seed)
+        return {"X": wl.as_dtype(inp["X"], dtype), "grid": wl.as_dtype(inp["grid"], dtype)}
+    if w.kind == "resize":
+        return {"X": wl.as_dtype(wl.make_resize_inputs(w, seed=seed)["X"], dtype)}
+    return {k: wl.as_dtype(v, dtype) for k, v in wl.make_deform_inputs(w, seed=seed).items()}
+
+
+def replica_seed(w, rank):
+    """Rank r of a replicated run draws its own images: the workload's seed + r."""
+    return w.seed + rank
+
+
+def max_over_ranks(x, world, device=None):
+    """The largest per-rank value over all ranks (the slowest replica sets the job's
+    time); x itself on one rank.  device is where the collective's tensor lives
+    (a CUDA device under NCCL, None for the CPU under gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(outputs_per_rank, world, ms):
+    """Whole-job throughput: every replica's outputs over the slowest replica's time."""
+    return outputs_per_rank * world / (ms * 1e-3)
 
 
 class ClockSampler:
@@ -185,7 +227,7 @@ class ClockSampler:
 class Case:
     """One workload on one device: inputs in HBM, a launch closure, byte/flop counts."""
 
-    def __init__(self, name, dtype, device, mode=None, seed_offset=0, workspace=False):
+    def __init__(self, name, dtype, device, mode=None, rank=0, workspace=False):
         import torch
         self.w = wl.WORKLOADS[name]
         self.name, self.dtype, self.device = name, dtype, device
@@ -194,13 +236,11 @@ class Case:
         self.launches = 1   # kernels per step
         w = self.w
         eb = DT_BYTES[dtype]
-        seed = w.seed + seed_offset
         import spatial_transformer_sampling_gb300 as gs
         self.gs = gs
+        self.host = host_inputs(w, dtype, replica_seed(w, rank))
         if w.kind == "affine_sample":
-            inp = wl.make_affine_sample_inputs(w, seed=seed)
-            self.host = {"theta": wl.as_dtype(inp["theta"], dtype), "X": wl.as_dtype(inp["X"], dtype)}
-            self.size = [int(s) for s in inp["size"]]
+            self.size = [w.x_shape[0], w.x_shape[1], *w.out_spatial]
             self.outputs = int(np.prod(self.size))
             if w.r == 2:
                 self.kernel_tag = f"band_kernel<{DT_SHORT[dtype]},{self.mode}>"
@@ -209,8 +249,6 @@ class Case:
             else:
                 self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},affine>"
         elif w.kind == "grid_sample":
-            inp = wl.make_grid_sample_inputs(w, seed=seed)
-            self.host = {"X": wl.as_dtype(inp["X"], dtype), "grid": wl.as_dtype(inp["grid"], dtype)}
             self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
             self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},grid>"
             if workspace:
@@ -223,15 +261,11 @@ class Case:
                     self.launches = 2 * (-(-w.x_shape[0] // per))   # copy + sample per chunk
                     self.kernel_tag = f"nhwc_sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
         elif w.kind == "resize":
-            inp = wl.make_resize_inputs(w, seed=seed)
-            self.host = {"X": wl.as_dtype(inp["X"], dtype)}
             self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
             self.resize_kw = dict(scales=list(w.extra["scales"]), mode=self.mode,
                                   antialias=w.extra["antialias"])
             self.kernel_tag = f"resize_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
         else:
-            inp = wl.make_deform_inputs(w, seed=seed)
-            self.host = {k: wl.as_dtype(v, dtype) for k, v in inp.items()}
             N, C, H, W_ = w.x_shape
             oH = (H + w.pads[0] + w.pads[2] - (w.kernel[0] - 1) - 1) // w.strides[0] + 1
             oW = (W_ + w.pads[1] + w.pads[3] - (w.kernel[1] - 1) - 1) // w.strides[1] + 1
@@ -287,11 +321,13 @@ def flush_l2(buf):
 
 
 def time_steps(case, steps, warmup, flush, barrier=None):
-    """Per-step CUDA-event durations (ms) of the hot path, L2 flushed before each step."""
+    """Per-step CUDA-event durations (ms) of the hot path, L2 flushed before each step
+    (flush None: steps back to back, warm L2)."""
     import torch
     stream = torch.cuda.current_stream(case.device)
     for _ in range(warmup):
-        flush_l2(flush)
+        if flush is not None:
+            flush_l2(flush)
         case.run()
     torch.cuda.synchronize(case.device)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -301,7 +337,8 @@ def time_steps(case, steps, warmup, flush, barrier=None):
     torch.cuda.synchronize(case.device)
     t0 = time.time()
     for i in range(steps):
-        flush_l2(flush)
+        if flush is not None:
+            flush_l2(flush)
         starts[i].record(stream)
         case.run()
         ends[i].record(stream)
@@ -387,7 +424,7 @@ def oracle_sample(case, budget_s=12.0):
     count (and cycling through the batch) until about budget_s of CPU time is spent."""
     import oracle
     w = case.w
-    threads = oracle.max_threads()
+    threads = oracle.num_procs()   # every host core, whatever OMP_NUM_THREADS says
     oracle.set_num_threads(threads)
     if not hasattr(case, "host64"):   # widen once; each step reuses it
         case.host64 = {k: wl.widened(v) for k, v in case.host.items()}
@@ -471,7 +508,7 @@ def main():
     pk = peaks()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
 
-    case = Case(args.workload, args.dtype, device, args.mode, seed_offset=rank,
+    case = Case(args.workload, args.dtype, device, args.mode, rank=rank,
                 workspace=args.workspace)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
@@ -481,19 +518,17 @@ def main():
     if sampler:
         sampler.stop()
     ms = sum(per_step) / len(per_step)
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = case.outputs * world / (ms_max * 1e-3)
+    ms_max = max_over_ranks(ms, world, device)
+    value = job_value(case.outputs, world, ms_max)
+    ms_median = max_over_ranks(statistics.median(per_step), world, device)
+
+    # warm L2: the same steps back to back with no flush in between
+    warm_steps, _, _ = time_steps(case, min(args.steps, 500), 5, None, barrier)
+    warm_ms = max_over_ranks(sum(warm_steps) / len(warm_steps), world, device)
 
     e2e_ms, h2d, d2h = time_e2e(case, max(5, min(50, args.steps // 10)), 3)
-    e2e_value = case.outputs * world / (e2e_ms * 1e-3)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = case.outputs * world / (float(t.item()) * 1e-3)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_value = job_value(case.outputs, world, e2e_ms)
 
     extra = []
     if rank == 0 and not args.no_extra:
@@ -522,19 +557,23 @@ def main():
             del c2
             torch.cuda.empty_cache()
 
-    cpu = oracle_sample(case) if rank == 0 else None
+    cpu = oracle_sample(case) if rank == 0 and world == 1 else None   # N=1 only
     if world > 1:
         dist.barrier()
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "ms_median": round(ms_median, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DT_SHORT[args.dtype], "data": "synthetic (seeded PCG64; no dataset)",
             "config": {"workload": workload_desc(case),
                        "l2": "flushed before every step: 512 MiB written then read (outside the timed interval)",
                        "parallelism": f"replicas x{world} (independent images, no collective)"},
             "roofline": roofline_for(case, ms, pk),
+            "warm_l2": {"value": round(job_value(case.outputs, world, warm_ms), 1), "unit": UNIT,
+                        "ms_per_step": round(warm_ms, 5), "steps": len(warm_steps),
+                        "note": "no flush between steps (inputs may stay in L2)"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -561,23 +600,14 @@ def reference_arm(args, rank, world):
     case = HostCase()
     case.w, case.name, case.dtype = w, args.workload, args.dtype
     case.mode = args.mode or w.mode
+    case.host = host_inputs(w, args.dtype, replica_seed(w, 0))
     if w.kind == "affine_sample":
-        inp = wl.make_affine_sample_inputs(w)
-        case.host = {"theta": wl.as_dtype(inp["theta"], args.dtype),
-                     "X": wl.as_dtype(inp["X"], args.dtype)}
-        case.size = [int(s) for s in inp["size"]]
-    elif w.kind == "grid_sample":
-        inp = wl.make_grid_sample_inputs(w)
-        case.host = {"X": wl.as_dtype(inp["X"], args.dtype), "grid": wl.as_dtype(inp["grid"], args.dtype)}
+        case.size = [w.x_shape[0], w.x_shape[1], *w.out_spatial]
     elif w.kind == "resize":
-        case.host = {"X": wl.as_dtype(wl.make_resize_inputs(w)["X"], args.dtype)}
         case.resize_kw = dict(scales=list(w.extra["scales"]), mode=case.mode,
                               antialias=w.extra["antialias"])
-    else:
-        inp = wl.make_deform_inputs(w)
-        case.host = {k: wl.as_dtype(v, args.dtype) for k, v in inp.items()}
     # the whole run stays within a few minutes: ~150 s of oracle time in all
-    per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    per_step_budget = min(args.sample_seconds, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(case, budget_s=per_step_budget / 4)
     vals = []

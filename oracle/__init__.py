@@ -115,6 +115,7 @@ def _bind(L):
                             ctypes.c_int, ctypes.c_double, ctypes.c_int, _f64p]
     L.or_set_num_threads.argtypes = [ctypes.c_int]
     L.or_max_threads.restype = ctypes.c_int
+    L.or_num_procs.restype = ctypes.c_int
     for f in ("or_affine_grid", "or_grid_sample", "or_grid_sample_at", "or_affine_sample",
               "or_affine_sample_at", "or_deform_conv", "or_deform_conv_at", "or_resize_shape",
               "or_resize"):
@@ -128,6 +129,10 @@ def set_num_threads(n):
 
 def max_threads():
     return int(lib().or_max_threads())
+
+
+def num_procs():
+    return int(lib().or_num_procs())
 
 
 def _f64(a):

@@ -53,6 +53,16 @@ int or_max_threads(void) {
 #endif
 }
 
+/* The host's processors as OpenMP sees them (unaffected by OMP_NUM_THREADS,
+   which launchers such as torchrun set to 1 for each rank). */
+int or_num_procs(void) {
+#ifdef _OPENMP
+    return omp_get_num_procs();
+#else
+    return 1;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* AffineGrid                                                                */
 /* ------------------------------------------------------------------------ */
