@@ -81,7 +81,7 @@ gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *s
  *
  *   X        device, (N, C, D1..Dr): values at pixel centres.
  *   x_shape  host, r+2 int64.
- *   r        1, 2 or 3 spatial dimensions.
+ *   r        1 to 6 spatial dimensions (GS_ERR_RANK otherwise).
  *   grid     device, (N, D1_out..Dr_out, r); the location vector lists the
  *            innermost axis first (x -> width, y -> height, z -> depth).
  *   out_spatial  host, r int64: D1_out..Dr_out.
@@ -97,7 +97,9 @@ gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *s
  *
  * The unnormalised coordinate is formed without rounding error (an exact
  * product split, then 32.32 fixed point), so nearest picks the same index as
- * exact arithmetic, ties included.
+ * exact arithmetic, ties included.  Ranks 4 to 6 run on one rank-general
+ * kernel (the tap product summed axis by axis, innermost first); the
+ * operator's description defines any rank r, and 6 is this library's limit.
  */
 gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const void *grid,
                          const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,

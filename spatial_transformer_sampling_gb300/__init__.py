@@ -9,7 +9,7 @@ call fails, an exception is raised.
 
 Operators (see the docstrings and include/gs.h):
   gs_affine_grid   AffineGrid
-  gs_grid_sample   GridSample (rank 1-3; linear / nearest / cubic;
+  gs_grid_sample   GridSample (rank 1-6; linear / nearest / cubic;
                    zeros / border / reflection; both align_corners)
   gs_affine_sample GridSample(X, AffineGrid(theta, size)) fused
   gs_deform_conv   DeformConv 2-D

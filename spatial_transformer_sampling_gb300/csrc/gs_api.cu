@@ -107,7 +107,7 @@ gs_status check_sample_shape(const int64_t *x_shape, int r, const int64_t *out_s
     if (N * tiles > kMaxSlab) return GS_ERR_SHAPE;
     args->N = (int)N;
     args->C = (int)C;
-    for (int d = 0; d < 3; ++d) {
+    for (int d = 0; d < gs::kMaxRankND; ++d) {
         args->in[d] = d < r ? (int)x_shape[2 + d] : 1;
         args->out[d] = d < r ? (int)out_sp[d] : 1;
     }
@@ -400,7 +400,7 @@ gs_status gs_affine_grid(const void *theta, gs_dtype dt, int r, const int64_t *s
 gs_status gs_grid_sample(const void *X, const int64_t *x_shape, int r, const void *grid,
                          const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
                          int align_corners, float cubic_coeff_a, void *Y, cudaStream_t stream) {
-    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (r < 1 || r > gs::kMaxRankND) return GS_ERR_RANK;
     gs::SampleArgs args;
     bool skip = false;
     gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,
@@ -419,7 +419,7 @@ gs_status gs_grid_sample_int(const void *X, gs_itype xt, const int64_t *x_shape,
                              const void *grid, gs_dtype grid_dt, const int64_t *out_spatial,
                              gs_mode mode, gs_pad pad, int align_corners, float cubic_coeff_a,
                              void *Y, cudaStream_t stream) {
-    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (r < 1 || r > gs::kMaxRankND) return GS_ERR_RANK;
     if (xt != GS_U8 && xt != GS_I8 && xt != GS_U16 && xt != GS_I16) return GS_ERR_DTYPE;
     gs::SampleArgs args;
     bool skip = false;
@@ -452,7 +452,7 @@ gs_status gs_grid_sample_workspace_size(const int64_t *x_shape, int r, const int
                                         gs_dtype dt, size_t *bytes) {
     if (!bytes) return GS_ERR_NULL;
     *bytes = 0;
-    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (r < 1 || r > gs::kMaxRankND) return GS_ERR_RANK;
     gs::SampleArgs args;
     bool skip = false;
     // mode and padding do not change the size: check the shapes only
@@ -471,7 +471,7 @@ gs_status gs_grid_sample_ws(const void *X, const int64_t *x_shape, int r, const 
                             const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
                             int align_corners, float cubic_coeff_a, void *workspace,
                             size_t workspace_bytes, void *Y, cudaStream_t stream) {
-    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (r < 1 || r > gs::kMaxRankND) return GS_ERR_RANK;
     gs::SampleArgs args;
     bool skip = false;
     gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,
@@ -492,7 +492,7 @@ gs_status gs_grid_sample_static(const void *X, const int64_t *x_shape, int r, co
                                 const int64_t *out_spatial, gs_dtype dt, gs_mode mode, gs_pad pad,
                                 int align_corners, float cubic_coeff_a, void *Y,
                                 cudaStream_t stream) {
-    if (r < 1 || r > 3) return GS_ERR_RANK;
+    if (r < 1 || r > gs::kMaxRankND) return GS_ERR_RANK;
     gs::SampleArgs args;
     bool skip = false;
     gs_status st = check_sample(X, x_shape, r, out_spatial, dt, mode, pad, align_corners,

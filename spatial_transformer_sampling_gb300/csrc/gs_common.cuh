@@ -117,6 +117,13 @@ __device__ __forceinline__ int64_t pos_to_q(double x, const Axis &A, int pad) {
     return __double2ll_rn(x * 4294967296.0);
 }
 
+// Element i of a grid of float type dt (0 fp32, 1 fp16, 2 bf16), widened to fp32.
+__device__ __forceinline__ float grid_value(const void *grid, int dt, int64_t i) {
+    if (dt == 0) return __ldg(reinterpret_cast<const float *>(grid) + i);
+    if (dt == 1) return __half2float(__ldg(reinterpret_cast<const __half *>(grid) + i));
+    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(grid) + i));
+}
+
 __device__ __forceinline__ int64_t clamp_q(int64_t x, int64_t lo, int64_t hi) {
     return x < lo ? lo : (x > hi ? hi : x);
 }

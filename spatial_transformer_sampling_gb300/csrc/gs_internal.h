@@ -12,10 +12,14 @@ constexpr int kSampleThreads = 256;
 struct Axis;   // gs_common.cuh
 
 // Arguments of the sampling kernels (GridSample and the fused affine path).
+// Largest spatial rank GridSample takes (ranks 4 and up run on one
+// rank-general kernel; the fused and channel-last paths take ranks 2 and 3).
+constexpr int kMaxRankND = 6;
+
 struct SampleArgs {
     int N, C;
-    int in[3];           // input spatial extents, outermost first (1 when unused)
-    int out[3];          // output spatial extents, outermost first
+    int in[kMaxRankND];  // input spatial extents, outermost first (1 when unused)
+    int out[kMaxRankND]; // output spatial extents, outermost first
     int64_t in_plane;    // product of in[]
     int64_t out_plane;   // product of out[]
     int tiles;           // blocks per image: ceil(out_plane / kSampleThreads)

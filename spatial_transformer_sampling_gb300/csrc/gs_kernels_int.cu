@@ -14,12 +14,6 @@
 
 namespace gs {
 
-__device__ __forceinline__ float grid_value(const void *grid, int dt, int64_t i) {
-    if (dt == 0) return __ldg(reinterpret_cast<const float *>(grid) + i);
-    if (dt == 1) return __half2float(__ldg(reinterpret_cast<const __half *>(grid) + i));
-    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(grid) + i));
-}
-
 template <typename TX, int R, int MODE>
 __global__ void __launch_bounds__(kSampleThreads)
 sample_int_kernel(const TX *__restrict__ X, const void *__restrict__ grid, int grid_dt,
@@ -72,6 +66,7 @@ static cudaError_t launch_int_r(const void *X, const void *grid, int grid_dt, vo
 template <typename TX>
 cudaError_t launch_sample_int(const void *X, const void *grid, int grid_dt, void *Y,
                               const SampleArgs &args, int r, int mode, cudaStream_t s) {
+    if (r > 3) return launch_sample_nd<TX>(X, grid, grid_dt, Y, args, r, mode, s);
     const SampleParams P = make_params<float>(args, r);
     if (r == 1) return launch_int_r<TX, 1>(X, grid, grid_dt, Y, P, mode, s);
     if (r == 2) return launch_int_r<TX, 2>(X, grid, grid_dt, Y, P, mode, s);

@@ -1,9 +1,9 @@
 // gs_sample.cuh -- GridSample and fused AffineGrid+GridSample kernels, and the
 // standalone AffineGrid kernel (templates; instantiated once per dtype).
 //
-// sample_kernel (any rank, tensor grid or fused affine; gs_band.cuh streams
+// sample_kernel (ranks 1-3, tensor grid or fused affine; gs_band.cuh streams
 // the fused 2-D case through shared memory instead, gs_vol.cuh the fused 3-D
-// trilinear and nearest cases): one thread per output
+// trilinear and nearest cases, gs_nd.cuh takes ranks 4 and up): one thread per output
 // position, looping over all C channels.  Coordinates, padding and tap
 // weights are computed once per position in registers and reused by every
 // channel (GridSample - version 20: the grid vector is shared by all channels
@@ -327,6 +327,7 @@ inline Axis make_axis(int n, int ac) {
 }  // namespace gs
 
 #include "gs_band.cuh"
+#include "gs_nd.cuh"
 #include "gs_nhwc.cuh"
 #include "gs_vol.cuh"
 
@@ -405,6 +406,7 @@ cudaError_t launch_sample(const void *X, const void *src, void *Y, const SampleA
         if (r == 2) return launch_sample_mode<T, 2, true>(X, src, Y, P, mode, s);
         return launch_sample_mode<T, 3, true>(X, src, Y, P, mode, s);
     }
+    if (r > 3) return launch_sample_nd<T>(X, src, grid_dt_of<T>(), Y, args, r, mode, s);
     if (ws && nhwc_workspace_bytes<T>(args, r, affine) > 0 &&
         ws_bytes >= nhwc_min_workspace_bytes<T>(args))
         return launch_nhwc<T>(X, src, Y, P, mode, ws, ws_bytes, s);

@@ -64,7 +64,7 @@ ENTRIES = ["gs_grid_sample", "gs_grid_sample_ws", "gs_grid_sample_static"]
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(mode=3), 5), (dict(pad=-1), 5), (dict(ac=2), 5), (dict(dt=9), 4),
-    (dict(r=4, x_shape=[1, 1, 2, 2, 2, 2], out=[2, 2, 2, 2]), 2), (dict(r=0), 2),
+    (dict(r=7, x_shape=[1, 1] + [2] * 7, out=[2] * 7), 2), (dict(r=0), 2),
     (dict(X=None), 1), (dict(Y=None), 1), (dict(grid=None), 1),
     (dict(X=FAKE + 2), 6), (dict(dt=1, Y=FAKE + 1), 6),
     (dict(x_shape=[1, 1, 1 << 21, 2]), 3), (dict(x_shape=[1, 1, -1, 2]), 3),
@@ -83,6 +83,16 @@ def test_grid_sample_rejects_bad_arguments(L, kwargs, status, entry):
 @pytest.mark.parametrize("entry", ENTRIES)
 def test_empty_tensors_return_ok_without_a_launch(L, x_shape, out, entry):
     assert _gsample(L, x_shape, out, X=None, grid=None, Y=None, entry=entry) == 0
+
+
+@pytest.mark.parametrize("r", [4, 5, 6])
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_ranks_four_to_six_are_accepted(L, r, entry):
+    # an empty output passes every check and returns without a launch
+    xs = [2, 3] + [4] * r
+    assert _gsample(L, xs, [0] + [3] * (r - 1), X=None, grid=None, Y=None, r=r, entry=entry) == 0
+    # a bad extent at the innermost axis is still caught
+    assert _gsample(L, [2, 3] + [4] * (r - 1) + [-1], [3] * r, r=r, entry=entry) == 3
 
 
 def test_static_scratch_rejects_an_image_slot_beyond_its_size(L):
@@ -215,7 +225,8 @@ def test_integer_x_entry_rejects_bad_types_on_the_host(L):
     # X type not an integer code, grid type not a float code, bad rank
     assert L.gs_grid_sample_int(FAKE, 0, xs, 2, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 4
     assert L.gs_grid_sample_int(FAKE, 16, xs, 2, FAKE, 9, out, 0, 0, 0, -0.75, FAKE, None) == 4
-    assert L.gs_grid_sample_int(FAKE, 16, xs, 4, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 2
+    assert L.gs_grid_sample_int(FAKE, 16, _i64([1, 2] + [4] * 7), 7, FAKE, 0, _i64([3] * 7), 0, 0,
+                                0, -0.75, FAKE, None) == 2
     # misaligned int16 X
     assert L.gs_grid_sample_int(FAKE + 1, 19, xs, 2, FAKE, 0, out, 0, 0, 0, -0.75, FAKE, None) == 6
     # empty output: no launch, no pointers needed

@@ -117,6 +117,85 @@ def test_tap_oracle_matches_dense_brute_force(oracle_mod, r, mode, pad, ac):
     np.testing.assert_allclose(Y, Yb, rtol=0, atol=1e-12)
 
 
+# ranks 4-6 (the operator's rank r+2 X, any r): every mode x padding x
+# align_corners at rank 4, a spread of them at ranks 5 and 6
+ND_CASES = ([(4, m, p, ac) for m in ("linear", "nearest", "cubic")
+             for p in ("zeros", "border", "reflection") for ac in (0, 1)] +
+            [(5, "linear", "reflection", 0), (5, "cubic", "border", 1), (5, "nearest", "zeros", 0),
+             (6, "linear", "zeros", 1), (6, "cubic", "reflection", 0), (6, "nearest", "border", 1)])
+
+
+@pytest.mark.parametrize("r,mode,pad,ac", ND_CASES)
+def test_tap_oracle_matches_dense_brute_force_rank_nd(oracle_mod, r, mode, pad, ac):
+    g = wl.rng(17 + 3 * r)
+    ins = {4: (3, 4, 2, 3), 5: (3, 2, 4, 2, 3), 6: (2, 3, 2, 2, 3, 2)}[r]
+    outs = {4: (3, 2, 2, 3), 5: (2, 2, 1, 2, 3), 6: (1, 2, 1, 2, 1, 2)}[r]
+    X = g.normal(size=(1, 2) + ins)
+    grid = g.uniform(-2.6, 2.6, size=(1,) + outs + (r,))
+    flat = grid.reshape(-1, r)
+    flat[:3] = np.array([-1.0, 1.0, 0.0])[:, None]
+    Y = oracle_mod.grid_sample(X, grid, mode, pad, ac)
+    Yb = _brute_grid_sample(X, grid, mode, pad, ac)
+    np.testing.assert_allclose(Y, Yb, rtol=0, atol=1e-12)
+
+
+def _positions(grid, ins, ac):
+    """Unnormalised positions, outermost axis first (the grid lists innermost first)."""
+    r = len(ins)
+    return [_unnorm(grid[..., r - 1 - d], ins[d], ac) for d in range(r)]
+
+
+def test_rank5_linear_reproduces_multilinear_functions(oracle_mod):
+    """N-linear interpolation is exact on functions that are affine in each
+    coordinate separately (products of ramps, plus ramps)."""
+    ins = (4, 3, 5, 3, 4)
+    c = np.array([0.3, -0.7, 0.2, 1.1, -0.4])
+    e = np.array([1.5, -0.25, 0.75, 0.5, -1.0])
+    idx = np.meshgrid(*[np.arange(n, dtype=np.float64) for n in ins], indexing="ij")
+
+    def f(p):
+        return np.prod([1.0 + c[d] * p[d] for d in range(5)], axis=0) + \
+            sum(e[d] * p[d] for d in range(5))
+
+    X = f(idx)[None, None]
+    grid = wl.rng(131).uniform(-1, 1, size=(1, 3, 4, 2, 3, 2, 5))
+    Y = oracle_mod.grid_sample(X, grid, "linear", "zeros", 1)
+    np.testing.assert_allclose(Y[0, 0], f(_positions(grid[0], ins, 1)), atol=1e-12)
+
+
+def test_rank4_cubic_reproduces_quadratics_at_a_minus_half(oracle_mod):
+    """Keys' kernel with a = -1/2 reproduces polynomials up to degree two on each
+    axis (Keys, 1981), so the tensor product reproduces sums of such products."""
+    ins = (7, 8, 7, 8)
+    idx = np.meshgrid(*[np.arange(n, dtype=np.float64) for n in ins], indexing="ij")
+
+    def f(p):
+        return (0.2 * p[0] * p[0] - 0.5 * p[0] * p[3] + 0.1 * p[1] * p[1] + p[2]
+                - 0.3 * p[1] * p[2] * p[3] + 0.05 * p[3] * p[3] * p[0] * p[0])
+
+    X = f(idx)[None, None]
+    grid = wl.rng(141).uniform(-0.4, 0.4, size=(1, 3, 2, 4, 3, 4))   # every tap inside
+    Y = oracle_mod.grid_sample(X, grid, "cubic", "zeros", 1, -0.5)
+    np.testing.assert_allclose(Y[0, 0], f(_positions(grid[0], ins, 1)), atol=1e-10)
+    Y75 = oracle_mod.grid_sample(X, grid, "cubic", "zeros", 1, -0.75)
+    assert np.abs(Y75[0, 0] - f(_positions(grid[0], ins, 1))).max() > 1e-3
+
+
+def test_rank6_nearest_picks_the_nearest_pixel(oracle_mod):
+    """Positions within 0.4 px of a pixel centre read that pixel, on every axis."""
+    ins = (3, 4, 2, 3, 4, 2)
+    g = wl.rng(151)
+    X = g.normal(size=(1, 2) + ins)
+    outs = (2, 3, 2, 2, 3, 2)
+    pick = np.stack([g.integers(0, ins[d], size=outs) for d in range(6)])     # outermost first
+    pos = pick + g.uniform(-0.4, 0.4, size=pick.shape)
+    # align_corners=0: x = ((g+1)*n - 1)/2  ->  g = (2x + 1)/n - 1
+    grid = np.stack([(2 * pos[d] + 1) / ins[d] - 1 for d in reversed(range(6))], -1)[None]
+    Y = oracle_mod.grid_sample(X, grid, "nearest", "zeros", 0)
+    for c in range(2):
+        np.testing.assert_array_equal(Y[0, c], X[0, c][tuple(pick)])
+
+
 @pytest.mark.parametrize("a", [-0.5, -0.75, -1.0])
 def test_cubic_coefficient_is_a_parameter(oracle_mod, a):
     g = wl.rng(3)
