@@ -81,74 +81,127 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
     const int npos = hn * Wo;
     const int tid = threadIdx.x;
 
-    if (tid < 32) build_affine_map_warp<T, 2>(theta + (int64_t)n * 6, P, s_map);
-    __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < kBandMaxStages; ++s) mbar_init(&full[s], 1);
-        fence_mbar_init();
-        // input row range of the band, from the four corners
-        int stages = 0, lo = 0, hi = 0;
-        if (!s_map.wide) {
-            int64_t ymin = INT64_MAX, ymax = INT64_MIN;
-            for (int ci = 0; ci < 4; ++ci) {
-                const int h = (ci & 1) ? h0 + hn - 1 : h0;
-                const int w = (ci & 2) ? Wo - 1 : 0;
-                const int64_t y = (s_map.cst_q[0] + s_map.coef_q[0][0] * h +
-                                   s_map.coef_q[0][1] * w) >> 8;
-                ymin = y < ymin ? y : ymin;
-                ymax = y > ymax ? y : ymax;
-            }
-            if (MODE != MODE_CUBIC && a.pad == PAD_BORDER) {
-                // linear/nearest clamp the coordinate before taking taps: a
-                // clamped position keeps its (zero-weight) second tap
-                ymin = clamp_q(ymin, 0, P.ax[0].hi_q);
-                ymax = clamp_q(ymax, 0, P.ax[0].hi_q);
-            }
-            lo = (int)(ymin >> 32) - (MODE == MODE_CUBIC ? 1 : 0);
-            hi = (int)(ymax >> 32) + (MODE == MODE_CUBIC ? 2 : 1);
-            if (a.pad == PAD_REFLECTION && (lo < 0 || hi > Hi - 1)) {
-                lo = 0;   // folded positions can land anywhere: take the plane
-                hi = Hi - 1;
-            }
-            // Border padding moves taps onto rows 0 and Hi-1, zeros padding
-            // masks taps outside; either way clamping both ends into range
-            // keeps every row a tap reads.
-            lo = min(max(lo, 0), Hi - 1);
-            hi = min(max(hi, 0), Hi - 1);
-            const int64_t stage = (int64_t)(hi - lo + 1) * Wi * (int64_t)sizeof(T) + kBandZeroPad;
-            stages = (int)min((int64_t)kBandMaxStages, (int64_t)B.ring_bytes / stage);
-            if (stages < kBandMinStages) stages = 0;
+    const T *Xn = X + (int64_t)n * a.C * a.in_plane;
+    if (tid < 32) {
+        // warp 0: the affine map, the band's input row range, the ring's
+        // split, and the first copies -- issued before the taps are set up,
+        // so the reads overlap that work
+        build_affine_map_warp<T, 2>(theta + (int64_t)n * 6, P, s_map);
+        __syncwarp();
+        const bool wide = s_map.wide;
+        // input row of the band's four corners, one lane each
+        int64_t y = 0;
+        if (tid < 4 && !wide) {
+            const int h = (tid & 1) ? h0 + hn - 1 : h0;
+            const int w = (tid & 2) ? Wo - 1 : 0;
+            y = (s_map.cst_q[0] + s_map.coef_q[0][0] * h + s_map.coef_q[0][1] * w) >> 8;
         }
-        s_r0 = lo;
-        s_rows = hi - lo + 1;
-        s_stages = stages;
-        s_abort = 0;
+        int64_t ymin = tid < 4 ? y : INT64_MAX, ymax = tid < 4 ? y : INT64_MIN;
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+            const int64_t a0 = __shfl_xor_sync(0xffffffffu, ymin, o);
+            const int64_t a1 = __shfl_xor_sync(0xffffffffu, ymax, o);
+            ymin = a0 < ymin ? a0 : ymin;
+            ymax = a1 > ymax ? a1 : ymax;
+        }
+        if (tid == 0) {
+            for (int s = 0; s < kBandMaxStages; ++s) mbar_init(&full[s], 1);
+            fence_mbar_init();
+            int stages = 0, lo = 0, hi = 0;
+            if (!wide) {
+                if (MODE != MODE_CUBIC && a.pad == PAD_BORDER) {
+                    // linear/nearest clamp the coordinate before taking taps: a
+                    // clamped position keeps its (zero-weight) second tap
+                    ymin = clamp_q(ymin, 0, P.ax[0].hi_q);
+                    ymax = clamp_q(ymax, 0, P.ax[0].hi_q);
+                }
+                lo = (int)(ymin >> 32) - (MODE == MODE_CUBIC ? 1 : 0);
+                hi = (int)(ymax >> 32) + (MODE == MODE_CUBIC ? 2 : 1);
+                if (a.pad == PAD_REFLECTION && (lo < 0 || hi > Hi - 1)) {
+                    lo = 0;   // folded positions can land anywhere: take the plane
+                    hi = Hi - 1;
+                }
+                // Border padding moves taps onto rows 0 and Hi-1, zeros padding
+                // masks taps outside; either way clamping both ends into range
+                // keeps every row a tap reads.
+                lo = min(max(lo, 0), Hi - 1);
+                hi = min(max(hi, 0), Hi - 1);
+                const int64_t stage =
+                    (int64_t)(hi - lo + 1) * Wi * (int64_t)sizeof(T) + kBandZeroPad;
+                stages = (int)min((int64_t)kBandMaxStages, (int64_t)B.ring_bytes / stage);
+                if (stages < kBandMinStages) stages = 0;
+            }
+            s_r0 = lo;
+            s_rows = hi - lo + 1;
+            s_stages = stages;
+            s_abort = 0;
+            if (stages) {
+                const uint32_t bytes = (uint32_t)(hi - lo + 1) * (uint32_t)Wi * (uint32_t)sizeof(T);
+                const T *Xr = Xn + (int64_t)lo * Wi;
+                for (int st = 0; st < stages && st < a.C; ++st) {
+                    mbar_arrive_expect_tx(&full[st], bytes);
+                    bulk_copy_g2s(band_smem + (size_t)st * (bytes + kBandZeroPad),
+                                  Xr + (int64_t)st * a.in_plane, bytes, &full[st]);
+                }
+            }
+        }
     }
     __syncthreads();
     const int S = s_stages;   // 0: gather from global
     const int r0 = s_r0, rows = s_rows;
     const uint32_t data_bytes = (uint32_t)rows * (uint32_t)Wi * (uint32_t)sizeof(T);
     const uint32_t stage_bytes = data_bytes + kBandZeroPad;
+    if (S) {
+        // zero pads (generic writes; the copies never touch them), made
+        // visible by the barrier after the taps
+        for (int e = tid; e < S * (kBandZeroPad / 4); e += kBandThreads) {
+            const int st = e / (kBandZeroPad / 4), k = e - st * (kBandZeroPad / 4);
+            *reinterpret_cast<uint32_t *>(band_smem + (size_t)st * stage_bytes + data_bytes + 4 * k) =
+                0u;
+        }
+    }
 
     // flattened taps of this thread's positions (tid, tid+256, ...: each
-    // channel's stores are whole lines per warp)
+    // channel's stores are whole lines per warp).  Position j+1 is position j
+    // plus kBandThreads: the output index advances by (dh, dw) with a carry
+    // into the row, and the 24.40 coordinates by the matching constants.
     uint32_t off[kBandPPT][NT];
     float wt[kBandPPT][NT];
     uint32_t okm[kBandPPT];
-    int pos[kBandPPT];
+    const int dh = kBandThreads / Wo, dw = kBandThreads - (kBandThreads / Wo) * Wo;
+    int h = h0 + tid / Wo, w = tid - (tid / Wo) * Wo;
+    const bool wide = s_map.wide;
+    int64_t yacc = 0, xacc = 0, ystep = 0, xstep = 0, ywrap = 0, xwrap = 0;
+    if (!wide) {
+        yacc = s_map.cst_q[0] + s_map.coef_q[0][0] * h + s_map.coef_q[0][1] * w;
+        xacc = s_map.cst_q[1] + s_map.coef_q[1][0] * h + s_map.coef_q[1][1] * w;
+        ystep = s_map.coef_q[0][0] * dh + s_map.coef_q[0][1] * dw;
+        xstep = s_map.coef_q[1][0] * dh + s_map.coef_q[1][1] * dw;
+        ywrap = s_map.coef_q[0][0] - s_map.coef_q[0][1] * Wo;
+        xwrap = s_map.coef_q[1][0] - s_map.coef_q[1][1] * Wo;
+    }
 #pragma unroll
     for (int j = 0; j < kBandPPT; ++j) {
         const int p = tid + j * kBandThreads;
-        pos[j] = p < npos ? p : -1;
-        const int pp = p < npos ? p : 0;
-        const int h = h0 + pp / Wo, w = pp - (pp / Wo) * Wo;
         int64_t yq, xq;
-        if (!s_map.wide) {
-            yq = (s_map.cst_q[0] + s_map.coef_q[0][0] * h + s_map.coef_q[0][1] * w) >> 8;
-            xq = (s_map.cst_q[1] + s_map.coef_q[1][0] * h + s_map.coef_q[1][1] * w) >> 8;
+        if (!wide) {
+            yq = yacc >> 8;   // 24.40 -> 32.32 (floor)
+            xq = xacc >> 8;
         } else {
-            yq = pos_to_q(s_map.cst[0] + s_map.coef[0][0] * h + s_map.coef[0][1] * w, P.ax[0], a.pad);
-            xq = pos_to_q(s_map.cst[1] + s_map.coef[1][0] * h + s_map.coef[1][1] * w, P.ax[1], a.pad);
+            const int hh = p < npos ? h : h0, ww = p < npos ? w : 0;
+            yq = pos_to_q(s_map.cst[0] + s_map.coef[0][0] * hh + s_map.coef[0][1] * ww, P.ax[0], a.pad);
+            xq = pos_to_q(s_map.cst[1] + s_map.coef[1][0] * hh + s_map.coef[1][1] * ww, P.ax[1], a.pad);
+        }
+        // next position
+        h += dh;
+        w += dw;
+        yacc += ystep;
+        xacc += xstep;
+        if (w >= Wo) {
+            w -= Wo;
+            h += 1;
+            yacc += ywrap;
+            xacc += xwrap;
         }
         AxisTaps<MODE> ty, tx;
         make_taps<MODE>(yq, P.ax[0], a.pad, a.ac, a.a, ty);
@@ -177,13 +230,13 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
 
     T *__restrict__ Yn = Y + (int64_t)n * a.C * a.out_plane + (int64_t)h0 * Wo;
     if (S == 0) {
-        const unsigned char *Xb =
-            reinterpret_cast<const unsigned char *>(X + (int64_t)n * a.C * a.in_plane);
+        const unsigned char *Xb = reinterpret_cast<const unsigned char *>(Xn);
         const int64_t in_bytes = a.in_plane * (int64_t)sizeof(T);
         for (int c = 0; c < a.C; ++c) {
 #pragma unroll
             for (int j = 0; j < kBandPPT; ++j) {
-                if (pos[j] < 0) continue;
+                const int p = tid + j * kBandThreads;
+                if (p >= npos) continue;
                 float acc = 0.0f;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
@@ -191,7 +244,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
                         ? IO<T>::ld(reinterpret_cast<const T *>(Xb + off[j][t])) : 0.0f;
                     acc = fmaf(wt[j][t], v, acc);
                 }
-                Yn[pos[j]] = IO<T>::st(acc);
+                Yn[p] = IO<T>::st(acc);
             }
             Xb += in_bytes;
             Yn += a.out_plane;
@@ -199,21 +252,8 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
         return;
     }
 
-    // zero pads (generic writes; the copies never touch them)
-    for (int e = tid; e < S * (kBandZeroPad / 4); e += kBandThreads) {
-        const int st = e / (kBandZeroPad / 4), k = e - st * (kBandZeroPad / 4);
-        *reinterpret_cast<uint32_t *>(band_smem + (size_t)st * stage_bytes + data_bytes + 4 * k) = 0u;
-    }
-    __syncthreads();
-
-    const T *Xr = X + (int64_t)n * a.C * a.in_plane + (int64_t)r0 * Wi;
-    if (tid == 0) {
-        for (int s = 0; s < S && s < a.C; ++s) {
-            mbar_arrive_expect_tx(&full[s], data_bytes);
-            bulk_copy_g2s(band_smem + (size_t)s * stage_bytes, Xr + (int64_t)s * a.in_plane,
-                          data_bytes, &full[s]);
-        }
-    }
+    __syncthreads();   // zero pads written
+    const T *Xr = Xn + (int64_t)r0 * Wi;
     const uint32_t ring = smem_u32(band_smem);
     int c = 0;
     int s = 0;
@@ -240,7 +280,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
                     float acc = 0.0f;
 #pragma unroll
                     for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
-                    Yn[pos[j]] = IO<T>::st(acc);
+                    Yn[tid + j * kBandThreads] = IO<T>::st(acc);
                 }
                 Yn += a.out_plane;
             }
@@ -276,7 +316,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
             float acc = 0.0f;
 #pragma unroll
             for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
-            if (pos[j] >= 0) Yn[pos[j]] = IO<T>::st(acc);
+            if (tid + j * kBandThreads < npos) Yn[tid + j * kBandThreads] = IO<T>::st(acc);
         }
         Yn += a.out_plane;
         __syncthreads();   // stage s fully read

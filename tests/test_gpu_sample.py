@@ -352,6 +352,27 @@ def test_affine_footprint_cases(gs_cuda, oracle_mod, mode, pad, ac, dtype):
         assert_parity(Y, ref, dtype, f"footprint {mode} {pad} ac={ac} {dtype}")
 
 
+@pytest.mark.parametrize("pad", ["zeros", "border", "reflection"])
+@pytest.mark.parametrize("mode", ["linear", "nearest", "cubic"])
+def test_affine_blocks_that_gather_from_global(gs_cuda, oracle_mod, pad, mode):
+    """Blocks whose input rows overflow the shared-memory ring (a 12x zoom-out
+    of a 300 x 256 image) and a map whose positions need fp64 (a translation
+    of millions of pixels) both gather from global memory."""
+    g = wl.rng(zlib.crc32(repr((pad, mode, "band-gather")).encode()))
+    xs = (2, 2, 300, 256)
+    size = (2, 2, 40, 64)
+    theta = np.array([[[12.0, 0.5, 0.0], [0.3, 11.0, 0.1]],
+                      [[1.0, 0.0, 3.0e6], [0.0, 1.0, -2.0e6]]])
+    Tt, Xt = wl.as_dtype(theta, "float32"), wl.as_dtype(g.normal(size=xs), "float32")
+    Y = gs_cuda.gs_affine_sample(Tt.cuda(), size, Xt.cuda(), mode, pad, 0)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, pad, 0)
+    if mode == "nearest":
+        assert_nearest_affine(oracle_mod, Y, ref, Tt, size, xs, 0)
+    else:
+        assert_parity(Y, ref, "float32", f"gather {mode} {pad}")
+
+
 @pytest.mark.parametrize("mode", ["linear", "cubic"])
 def test_affine_tall_input_zoomed_and_transposed(gs_cuda, oracle_mod, mode):
     g = wl.rng(17)
