@@ -30,11 +30,21 @@ constexpr int kBandMaxStages = 16;
 constexpr int kBandMinStages = 2;
 constexpr int kBandZeroPad = 16;     // bytes of zeros after each stage's rows
 
-// Blocks per SM the register allocation must allow: 4 for linear and nearest
-// (a 64-register budget, which their taps fit); cubic's 16 taps per position
-// need more registers than that, so it runs fewer, larger blocks.
-template <int MODE> struct BandMinBlocks { static constexpr int value = 4; };
-template <> struct BandMinBlocks<MODE_CUBIC> { static constexpr int value = 1; };
+// Blocks per SM and shared-memory ring per block.  Linear and nearest on
+// 16-bit types: 4 blocks of 48 KB (a 64-register budget, which their taps
+// fit).  On fp32 a stage is twice as large, so the same ring holds half as
+// many channels in flight; 3 blocks of 72 KB keep more of them in flight and
+// measure faster (stn2d fp32: 53.9 -> 52.1 us), while 16-bit types lose more
+// to the lower occupancy than they gain.  Cubic's 16 taps per position need
+// more registers: one block per SM.
+template <typename T, int MODE> struct BandCfg {
+    static constexpr int min_blocks = sizeof(T) == 4 ? 3 : 4;
+    static constexpr int ring = sizeof(T) == 4 ? 72 * 1024 : 48 * 1024;
+};
+template <typename T> struct BandCfg<T, MODE_CUBIC> {
+    static constexpr int min_blocks = 1;
+    static constexpr int ring = 48 * 1024;
+};
 
 struct BandParams {
     int th;            // output rows per band
@@ -61,8 +71,32 @@ template <> __device__ __forceinline__ float lds_at<__nv_bfloat16>(uint32_t addr
     return __uint_as_float((uint32_t)v << 16);
 }
 
-template <typename T, int MODE>
-__global__ void __launch_bounds__(kBandThreads, BandMinBlocks<MODE>::value)
+// Two adjacent outputs from an fp32 pair, each rounded to nearest even as
+// IO<T>::st rounds it, in one store (p is aligned to two elements).
+template <typename T> __device__ __forceinline__ void st_pair(T *p, float2 v);
+template <> __device__ __forceinline__ void st_pair<float>(float *p, float2 v) {
+    *reinterpret_cast<float2 *>(p) = v;
+}
+template <> __device__ __forceinline__ void st_pair<__half>(__half *p, float2 v) {
+    *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(v.x, v.y);
+}
+template <> __device__ __forceinline__ void st_pair<__nv_bfloat16>(__nv_bfloat16 *p, float2 v) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
+
+// PAIRS: how a thread's outputs share packed fp32 FMAs (fma.rn.f32x2; each
+// lane rounds exactly as fmaf does).
+//   kPairNone     outputs t, t+256, t+512, t+768, one FMA per tap each;
+//   kPairAdjacent outputs 2t, 2t+1, 2t+512, 2t+513: a pair shares one FMA per
+//                 tap, one conversion and one store (16-bit types; needs an
+//                 even output width and Y aligned to two elements; for fp32
+//                 the lanes' 8-byte-apart loads would conflict in the banks);
+//   kPairStrided  outputs t, t+256, ...: t and t+256 share one FMA per tap,
+//                 stored apart (fp32).
+enum { kPairNone = 0, kPairAdjacent = 1, kPairStrided = 2 };
+
+template <typename T, int MODE, int PAIRS>
+__global__ void __launch_bounds__(kBandThreads, BandCfg<T, MODE>::min_blocks)
 band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict__ Y,
             const SampleParams P, const BandParams B) {
     constexpr int K = TapCount<MODE>::K;
@@ -161,28 +195,41 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
         }
     }
 
-    // flattened taps of this thread's positions (tid, tid+256, ...: each
-    // channel's stores are whole lines per warp).  Position j+1 is position j
-    // plus kBandThreads: the output index advances by (dh, dw) with a carry
+    // flattened taps of this thread's positions (each channel's stores are
+    // whole lines per warp).  Consecutive positions of a thread are a fixed
+    // distance apart (kBandThreads; for adjacent pairs alternately 1 and
+    // 2*kBandThreads-1): the output index advances by (dh, dw) with a carry
     // into the row, and the 24.40 coordinates by the matching constants.
     uint32_t off[kBandPPT][NT];
     float wt[kBandPPT][NT];
     uint32_t okm[kBandPPT];
-    const int dh = kBandThreads / Wo, dw = kBandThreads - (kBandThreads / Wo) * Wo;
-    int h = h0 + tid / Wo, w = tid - (tid / Wo) * Wo;
+    // position of this thread's j-th output within the band
+    constexpr bool kAdj = PAIRS == kPairAdjacent;
+    auto pos_of = [&](int j) {
+        return kAdj ? 2 * tid + (j & 1) + (j >> 1) * (2 * kBandThreads) : tid + j * kBandThreads;
+    };
+    constexpr int kStepA = kAdj ? 1 : kBandThreads;                      // after even j
+    constexpr int kStepB = kAdj ? 2 * kBandThreads - 1 : kBandThreads;   // after odd j
+    const int dhA = kStepA / Wo, dwA = kStepA - (kStepA / Wo) * Wo;
+    const int dhB = kStepB / Wo, dwB = kStepB - (kStepB / Wo) * Wo;
+    const int p0 = pos_of(0);
+    int h = h0 + p0 / Wo, w = p0 - (p0 / Wo) * Wo;
     const bool wide = s_map.wide;
-    int64_t yacc = 0, xacc = 0, ystep = 0, xstep = 0, ywrap = 0, xwrap = 0;
+    int64_t yacc = 0, xacc = 0, ystepA = 0, xstepA = 0, ystepB = 0, xstepB = 0, ywrap = 0,
+            xwrap = 0;
     if (!wide) {
         yacc = s_map.cst_q[0] + s_map.coef_q[0][0] * h + s_map.coef_q[0][1] * w;
         xacc = s_map.cst_q[1] + s_map.coef_q[1][0] * h + s_map.coef_q[1][1] * w;
-        ystep = s_map.coef_q[0][0] * dh + s_map.coef_q[0][1] * dw;
-        xstep = s_map.coef_q[1][0] * dh + s_map.coef_q[1][1] * dw;
+        ystepA = s_map.coef_q[0][0] * dhA + s_map.coef_q[0][1] * dwA;
+        xstepA = s_map.coef_q[1][0] * dhA + s_map.coef_q[1][1] * dwA;
+        ystepB = s_map.coef_q[0][0] * dhB + s_map.coef_q[0][1] * dwB;
+        xstepB = s_map.coef_q[1][0] * dhB + s_map.coef_q[1][1] * dwB;
         ywrap = s_map.coef_q[0][0] - s_map.coef_q[0][1] * Wo;
         xwrap = s_map.coef_q[1][0] - s_map.coef_q[1][1] * Wo;
     }
 #pragma unroll
     for (int j = 0; j < kBandPPT; ++j) {
-        const int p = tid + j * kBandThreads;
+        const int p = pos_of(j);
         int64_t yq, xq;
         if (!wide) {
             yq = yacc >> 8;   // 24.40 -> 32.32 (floor)
@@ -193,10 +240,11 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
             xq = pos_to_q(s_map.cst[1] + s_map.coef[1][0] * hh + s_map.coef[1][1] * ww, P.ax[1], a.pad);
         }
         // next position
-        h += dh;
-        w += dw;
-        yacc += ystep;
-        xacc += xstep;
+        const bool stepA = (j & 1) == 0;
+        h += stepA ? dhA : dhB;
+        w += stepA ? dwA : dwB;
+        yacc += stepA ? ystepA : ystepB;
+        xacc += stepA ? xstepA : xstepB;
         if (w >= Wo) {
             w -= Wo;
             h += 1;
@@ -235,7 +283,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
         for (int c = 0; c < a.C; ++c) {
 #pragma unroll
             for (int j = 0; j < kBandPPT; ++j) {
-                const int p = tid + j * kBandThreads;
+                const int p = pos_of(j);
                 if (p >= npos) continue;
                 float acc = 0.0f;
 #pragma unroll
@@ -251,6 +299,38 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
         }
         return;
     }
+
+    // One channel from the stage at `base`: every position of this thread
+    // (full: the band is whole, no bounds checks).
+    auto channel_out = [&](uint32_t base, T *__restrict__ Yc, bool full) {
+        if constexpr (PAIRS != kPairNone) {
+#pragma unroll
+            for (int jp = 0; jp < kBandPPT / 2; ++jp) {
+                const int j0 = 2 * jp, j1 = 2 * jp + 1;
+                float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    acc = fma_f32x2(make_float2(wt[j0][t], wt[j1][t]),
+                                    make_float2(lds_at<T>(base + off[j0][t]),
+                                                lds_at<T>(base + off[j1][t])),
+                                    acc);
+                if constexpr (kAdj) {
+                    if (full || pos_of(j0) < npos) st_pair<T>(Yc + pos_of(j0), acc);
+                } else {
+                    if (full || pos_of(j0) < npos) Yc[pos_of(j0)] = IO<T>::st(acc.x);
+                    if (full || pos_of(j1) < npos) Yc[pos_of(j1)] = IO<T>::st(acc.y);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kBandPPT; ++j) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
+                if (full || pos_of(j) < npos) Yc[pos_of(j)] = IO<T>::st(acc);
+            }
+        }
+    };
 
     __syncthreads();   // zero pads written
     const T *Xr = Xn + (int64_t)r0 * Wi;
@@ -275,13 +355,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const uint32_t base = ring + (uint32_t)(k ? s2 : s) * stage_bytes;
-#pragma unroll
-                for (int j = 0; j < kBandPPT; ++j) {
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
-                    Yn[tid + j * kBandThreads] = IO<T>::st(acc);
-                }
+                channel_out(base, Yn, true);
                 Yn += a.out_plane;
             }
             __syncthreads();   // both stages fully read
@@ -311,13 +385,7 @@ band_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restrict_
         __syncthreads();   // every thread has waited (or given up) on stage s
         if (s_abort) break;
         const uint32_t base = ring + (uint32_t)s * stage_bytes;
-#pragma unroll
-        for (int j = 0; j < kBandPPT; ++j) {
-            float acc = 0.0f;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) acc = fmaf(wt[j][t], lds_at<T>(base + off[j][t]), acc);
-            if (tid + j * kBandThreads < npos) Yn[tid + j * kBandThreads] = IO<T>::st(acc);
-        }
+        channel_out(base, Yn, false);
         Yn += a.out_plane;
         __syncthreads();   // stage s fully read
         if (tid == 0 && c + S < a.C) {
@@ -351,25 +419,33 @@ cudaError_t launch_band(const void *X, const void *theta, void *Y, const SampleP
     const size_t row_bytes = (size_t)Wi * sizeof(T);
     if (row_bytes % 16 != 0 || (uintptr_t)X % 16 != 0) return cudaSuccess;
     if (Wo > kBandThreads * kBandPPT) return cudaSuccess;
-    constexpr int kRingBytes = 48 * 1024;   // four blocks per SM (with the register bound)
+    constexpr int kRingBytes = BandCfg<T, MODE>::ring;
     if ((size_t)kRingBytes < (size_t)kBandMinStages * (4 * row_bytes + kBandZeroPad))
         return cudaSuccess;                 // rows too wide to stage usefully
     BandParams B;
     B.th = min(a.out[0], (kBandThreads * kBandPPT) / Wo);
     B.bands = (a.out[0] + B.th - 1) / B.th;
     B.ring_bytes = kRingBytes;
-    static bool attr_set[64] = {};
+    // packed FMAs for linear and nearest: fp32 pairs outputs t and t+256;
+    // 16-bit types pair adjacent outputs when the width is even and Y is
+    // aligned to a pair
+    constexpr int kPairs = MODE == MODE_CUBIC ? kPairNone
+                           : (sizeof(T) == 4 ? kPairStrided : kPairAdjacent);
+    const bool pairs = kPairs == kPairStrided ||
+                       (kPairs == kPairAdjacent && Wo % 2 == 0 &&
+                        (uintptr_t)Y % (2 * sizeof(T)) == 0);
+    auto kern = pairs ? band_kernel<T, MODE, kPairs> : band_kernel<T, MODE, kPairNone>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            band_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (dev < 64 && !attr_set[pairs][dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[pairs][dev] = true;
     }
     const unsigned blocks = (unsigned)((int64_t)a.N * B.bands);
-    band_kernel<T, MODE><<<blocks, kBandThreads, kRingBytes, s>>>((const T *)X, (const T *)theta,
-                                                                   (T *)Y, P, B);
+    kern<<<blocks, kBandThreads, kRingBytes, s>>>((const T *)X, (const T *)theta, (T *)Y, P, B);
     *used = true;
     return cudaGetLastError();
 }

@@ -387,6 +387,28 @@ def test_affine_tall_input_zoomed_and_transposed(gs_cuda, oracle_mod, mode):
         assert gs_cuda.gs_device_status() == 0
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("mode", ["linear", "nearest"])
+def test_output_pairs_match_single_outputs(gs_cuda, oracle_mod, dtype, mode):
+    """Even output widths with Y aligned to two elements take adjacent output
+    pairs per thread (packed FMA, one store per pair); a Y one element off that
+    alignment takes one output at a time.  Same bits either way."""
+    w = wl.WORKLOADS["stn2d"]
+    inp = wl.make_affine_sample_inputs(w, x_shape=(6, 5, 128, 128), out_spatial=(50, 128))
+    Tt, Xt = wl.as_dtype(inp["theta"], dtype).cuda(), wl.as_dtype(inp["X"], dtype).cuda()
+    size = (6, 5, 50, 128)
+    Y1 = gs_cuda.gs_affine_sample(Tt, size, Xt, mode, "border", 1)
+    buf = torch.empty(Y1.numel() + 1, dtype=Y1.dtype, device="cuda")
+    Y2 = buf[1:].view(size)
+    gs_cuda.gs_affine_sample(Tt, size, Xt, mode, "border", 1, out=Y2)
+    assert torch.equal(Y1, Y2)
+    ref = oracle_mod.affine_sample(exact(Tt), size, exact(Xt), mode, "border", 1)
+    if mode == "nearest":
+        assert_nearest_affine(oracle_mod, Y1, ref, Tt.cpu(), size, (6, 5, 128, 128), 1)
+    else:
+        assert_parity(Y1, ref, dtype, f"pairs {dtype}")
+
+
 def test_results_do_not_depend_on_input_alignment(gs_cuda):
     """An X view offset by one element gives bit-identical results."""
     w = wl.WORKLOADS["stn2d"]
