@@ -18,6 +18,10 @@
 // allows (up to 16).  A band whose rows do not fit two stages (strong
 // zoom-out, large rotation, reflection of far-out positions) or whose map
 // needs fp64 gathers from global memory instead, with the same taps.
+//
+// Warp 0 builds the map, finds the row range and issues the first stages
+// before the block sets up its taps, so those reads overlap the setup.  A
+// thread's outputs are paired on packed fp32 FMAs (see PAIRS below).
 #pragma once
 
 #include "gs_ptx.cuh"
