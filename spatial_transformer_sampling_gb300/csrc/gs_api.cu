@@ -366,6 +366,7 @@ gs_status gs_resize(const void *X, int rank, const int64_t *x_shape, const int64
         resize_taps_per_axis(attrs, P.scale[d], &A);
         if (A.taps > gs::kRsMaxTapsHost) return GS_ERR_UNSUPPORTED;
     }
+    a.err = error_word();
     return dispatch(dt, [&](auto tag) {
         return gs::launch_resize<decltype(tag)>(X, Y, a, stream);
     });

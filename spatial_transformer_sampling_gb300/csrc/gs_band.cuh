@@ -56,25 +56,6 @@ struct BandParams {
     int ring_bytes;    // shared-memory ring, split into stages per band
 };
 
-// Shared-memory load at a 32-bit shared address (volatile: never moved across
-// the stage waits and barriers).
-template <typename T> __device__ __forceinline__ float lds_at(uint32_t addr);
-template <> __device__ __forceinline__ float lds_at<float>(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-template <> __device__ __forceinline__ float lds_at<__half>(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return __half2float(__ushort_as_half(v));
-}
-template <> __device__ __forceinline__ float lds_at<__nv_bfloat16>(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return __uint_as_float((uint32_t)v << 16);
-}
-
 // Two adjacent outputs from an fp32 pair, each rounded to nearest even as
 // IO<T>::st rounds it, in one store (p is aligned to two elements).
 template <typename T> __device__ __forceinline__ void st_pair(T *p, float2 v);

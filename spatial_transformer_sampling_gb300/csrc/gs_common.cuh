@@ -70,6 +70,25 @@ template <> struct IO<int8_t> : IntIO<int8_t, -128, 127> {};
 template <> struct IO<uint16_t> : IntIO<uint16_t, 0, 65535> {};
 template <> struct IO<int16_t> : IntIO<int16_t, -32768, 32767> {};
 
+// Shared-memory load at a 32-bit shared address (volatile: never moved across
+// the stage waits and barriers).
+template <typename T> __device__ __forceinline__ float lds_at(uint32_t addr);
+template <> __device__ __forceinline__ float lds_at<float>(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+template <> __device__ __forceinline__ float lds_at<__half>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __half2float(__ushort_as_half(v));
+}
+template <> __device__ __forceinline__ float lds_at<__nv_bfloat16>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __uint_as_float((uint32_t)v << 16);
+}
+
 // ------------------------------------------------------------- axis params
 
 // One input spatial axis, precomputed on the host.

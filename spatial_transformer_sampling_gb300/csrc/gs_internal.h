@@ -71,6 +71,7 @@ struct ResizeArgs {
     double a;
     int exclude_outside;
     float extrapolation_value;
+    unsigned *err;   // device error word (bounded waits record timeouts here)
 };
 
 // Per-dtype launchers; T is float, __half or __nv_bfloat16.  Each enqueues on

@@ -25,6 +25,7 @@
 
 #include "gs_common.cuh"
 #include "gs_internal.h"
+#include "gs_ptx.cuh"
 
 namespace gs {
 
@@ -463,21 +464,17 @@ resize_rows_kernel(const T *__restrict__ X, T *__restrict__ Y, const __grid_cons
     }
 }
 
-// Row kernel for r <= 2 and fixed tap counts when the tables fit the kernel
-// parameters; *used reports whether it ran.
-template <typename T>
-cudaError_t launch_resize_rows(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s,
-                               bool *used) {
-    *used = false;
-    if (p.r > 2) return cudaSuccess;
+// Per-axis tap tables of the row kernels (r <= 2, fixed tap counts): false
+// when they do not fit the kernel parameters.
+inline bool build_resize_tables(const ResizeArgs &p, ResizeTables &tb) {
+    if (p.r > 2) return false;
     const ResizeAxis &AX = p.ax[2], &AY = p.ax[1];
     const int kx = AX.taps, ky = p.r == 2 ? AY.taps : 1;
     const bool ok_taps = (p.r == 2 && kx == ky && (kx == 1 || kx == 2 || kx == 4)) ||
                          (p.r == 1 && (kx == 1 || kx == 2 || kx == 4));
-    if (!ok_taps || AX.n_out > kRsThreads * kRsRowsMaxCols) return cudaSuccess;
+    if (!ok_taps || AX.n_out > kRsThreads * kRsRowsMaxCols) return false;
     const int nx = AX.n_out, ny = p.r == 2 ? AY.n_out : 1;
-    if (rs_table_bytes(nx, kx, ny, ky) > (size_t)kRsTableBytes) return cudaSuccess;
-    ResizeTables tb;
+    if (rs_table_bytes(nx, kx, ny, ky) > (size_t)kRsTableBytes) return false;
     tb.nx = nx;
     tb.ny = ny;
     tb.kx = kx;
@@ -512,6 +509,26 @@ cudaError_t launch_resize_rows(const void *X, void *Y, const ResizeArgs &p, cuda
             yw[o * ky + k] = c < 0 ? 0.0f : wb[k];
         }
     }
+    return true;
+}
+
+template <typename T, int KY, int KX>
+static void launch_rows_kernel(const T *X, T *Y, const ResizeTables &tb, const ResizeArgs &p,
+                               dim3 grid, int rows, int per, cudaStream_t s) {
+    const int H = p.r == 2 ? p.ax[1].n_in : 1, W = p.ax[2].n_in;
+    resize_rows_kernel<T, KY, KX><<<grid, kRsThreads, 0, s>>>(X, Y, tb, p.B, H, W, rows, per,
+                                                              p.extrapolation_value);
+}
+
+// Row kernel for r <= 2 and fixed tap counts when the tables fit the kernel
+// parameters; *used reports whether it ran.
+template <typename T>
+cudaError_t launch_resize_rows(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s,
+                               bool *used) {
+    *used = false;
+    ResizeTables tb;
+    if (!build_resize_tables(p, tb)) return cudaSuccess;
+    const int ny = tb.ny, kx = tb.kx, ky = tb.ky;
     // enough blocks for several waves: bands of rows x chunks of slices
     int rows = 8;
     int64_t per = 64;
@@ -522,24 +539,290 @@ cudaError_t launch_resize_rows(const void *X, void *Y, const ResizeArgs &p, cuda
     while (rows > 1 && blocks(rows, per) < 8 * 152) rows >>= 1;
     per = std::max<int64_t>(per, (p.B + 65534) / 65535);
     const dim3 grid((unsigned)((ny + rows - 1) / rows), (unsigned)((p.B + per - 1) / per));
-    const int H = p.r == 2 ? AY.n_in : 1, W = AX.n_in;
-    if (kx == 1 && ky == 1)
-        resize_rows_kernel<T, 1, 1><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
-                                                                rows, (int)per, p.extrapolation_value);
-    else if (ky == 1 && kx == 2)
-        resize_rows_kernel<T, 1, 2><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
-                                                                rows, (int)per, p.extrapolation_value);
-    else if (ky == 1 && kx == 4)
-        resize_rows_kernel<T, 1, 4><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
-                                                                rows, (int)per, p.extrapolation_value);
-    else if (kx == 2)
-        resize_rows_kernel<T, 2, 2><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
-                                                                rows, (int)per, p.extrapolation_value);
-    else
-        resize_rows_kernel<T, 4, 4><<<grid, kRsThreads, 0, s>>>((const T *)X, (T *)Y, tb, p.B, H, W,
-                                                                rows, (int)per, p.extrapolation_value);
+    const T *x = (const T *)X;
+    T *y = (T *)Y;
+    if (kx == 1 && ky == 1) launch_rows_kernel<T, 1, 1>(x, y, tb, p, grid, rows, (int)per, s);
+    else if (ky == 1 && kx == 2) launch_rows_kernel<T, 1, 2>(x, y, tb, p, grid, rows, (int)per, s);
+    else if (ky == 1 && kx == 4) launch_rows_kernel<T, 1, 4>(x, y, tb, p, grid, rows, (int)per, s);
+    else if (kx == 2) launch_rows_kernel<T, 2, 2>(x, y, tb, p, grid, rows, (int)per, s);
+    else launch_rows_kernel<T, 4, 4>(x, y, tb, p, grid, rows, (int)per, s);
     *used = true;
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------
+// Staged row kernel: the row kernel's tables and loop, with a slice's input
+// rows copied into shared memory first.  A block owns a band of output rows
+// (full width) for a range of slices.  The rows the band's taps read form
+// one contiguous range of every slice, so one bulk async copy per slice
+// (counted on an mbarrier) fills a stage of a ring; the taps are then
+// shared-memory loads instead of cached global gathers.  The arithmetic (and
+// so every bit of the result) is the row kernel's.
+
+constexpr int kRsStageRing = 48 * 1024;   // four blocks per SM
+constexpr int kRsStageMax = 16;
+constexpr int kRsStageRows = 32;          // output rows per band, at most
+
+template <typename T, int KY, int KX, int G>
+__global__ void __launch_bounds__(kRsThreads, 4)
+resize_stage_kernel(const T *__restrict__ X, T *__restrict__ Y,
+                    const __grid_constant__ ResizeTables tb, int64_t B, int H, int W,
+                    int rows_per_block, int slices_per_block, float extrapolation_value,
+                    unsigned *err) {
+    extern __shared__ __align__(128) unsigned char rs_smem[];
+    __shared__ __align__(8) uint64_t full[kRsStageMax];
+    __shared__ int s_r0, s_rows, s_stages, s_abort;
+    // the band's row taps: byte offsets within a stage, weights, flags (read
+    // once here rather than from the parameter table for every slice)
+    __shared__ uint32_t s_ry[kRsStageRows * KY];
+    __shared__ float s_wy[kRsStageRows * KY];
+    __shared__ int s_fy[kRsStageRows];
+    const int nx = tb.nx, ny = tb.ny;
+    const int *xi = reinterpret_cast<const int *>(tb.data);
+    const float *xw = reinterpret_cast<const float *>(tb.data + (size_t)nx * KX * 4);
+    const int *yi = reinterpret_cast<const int *>(tb.data + (size_t)nx * KX * 8);
+    const float *yw = reinterpret_cast<const float *>(tb.data + (size_t)nx * KX * 8 + (size_t)ny * KY * 4);
+    const unsigned char *xf = tb.data + ((size_t)nx * KX + (size_t)ny * KY) * 8;
+    const unsigned char *yf = xf + nx;
+
+    const int y0 = blockIdx.x * rows_per_block;
+    const int y1 = min(ny, y0 + rows_per_block);
+    const int64_t b0 = (int64_t)blockIdx.y * slices_per_block;
+    const int nb = (int)(min(B, b0 + slices_per_block) - b0);
+    const int tid = threadIdx.x;
+    const int64_t in_slice = (int64_t)H * W, out_slice = (int64_t)ny * nx;
+    const uint32_t row_bytes = (uint32_t)W * (uint32_t)sizeof(T);
+
+    if (tid == 0) {
+        // input rows of the band's taps (rows set to extrapolation_value read none)
+        int lo = 0x7fffffff, hi = -1;
+        for (int y = y0; y < y1; ++y) {
+            if (yf[y]) continue;
+            for (int k = 0; k < KY; ++k) {
+                lo = min(lo, yi[y * KY + k]);
+                hi = max(hi, yi[y * KY + k]);
+            }
+        }
+        if (hi < 0) lo = hi = 0;
+        const uint32_t stage = (uint32_t)(hi - lo + 1) * row_bytes;
+        const int stages = min(kRsStageMax, (int)(kRsStageRing / stage));   // >= 2 (host)
+        for (int st = 0; st < kRsStageMax; ++st) mbar_init(&full[st], 1);
+        fence_mbar_init();
+        const T *src = X + b0 * in_slice + (int64_t)lo * W;
+        for (int st = 0; st < stages && st < nb; ++st) {
+            mbar_arrive_expect_tx(&full[st], stage);
+            bulk_copy_g2s(rs_smem + (size_t)st * stage, src + (int64_t)st * in_slice, stage, &full[st]);
+        }
+        s_r0 = lo;
+        s_rows = hi - lo + 1;
+        s_stages = stages;
+        s_abort = 0;
+    }
+
+    // this thread's columns: byte offsets of their taps within a row, weights
+    uint32_t cx[kRsRowsMaxCols][KX];
+    float cw[kRsRowsMaxCols][KX];
+    bool cf[kRsRowsMaxCols];
+    int ncols = 0;
+#pragma unroll
+    for (int j = 0; j < kRsRowsMaxCols; ++j) {
+        const int x = tid + j * kRsThreads;
+        const bool in = x < nx;
+        if (in) ncols = j + 1;
+#pragma unroll
+        for (int k = 0; k < KX; ++k) {
+            cx[j][k] = in ? (uint32_t)xi[x * KX + k] * (uint32_t)sizeof(T) : 0u;
+            cw[j][k] = in ? xw[x * KX + k] : 0.0f;
+        }
+        cf[j] = in && xf[x];
+    }
+    __syncthreads();
+    const int S = s_stages, r0 = s_r0;
+    const uint32_t stage_bytes = (uint32_t)s_rows * row_bytes;
+    for (int e = tid; e < (y1 - y0) * KY; e += kRsThreads) {
+        const int y = y0 + e / KY, k = e - (e / KY) * KY;
+        // rows set to extrapolation_value never read their (zero) offsets
+        s_ry[e] = yf[y] ? 0u : (uint32_t)(yi[y * KY + k] - r0) * row_bytes;
+        s_wy[e] = yw[y * KY + k];
+        if (k == 0) s_fy[e / KY] = yf[y];
+    }
+    __syncthreads();
+    const uint32_t ring = smem_u32(rs_smem);
+    const T *src = X + b0 * in_slice + (int64_t)r0 * W;
+    const T ext = IO<T>::st(extrapolation_value);
+
+    // G slices per pass (their stages land, are read and are refilled
+    // together), so each row's taps are read once for all G; the host picks
+    // G <= S/2, which keeps the next group's copies in flight meanwhile
+    int st = 0;
+    uint32_t parity = 0;
+    int c = 0;
+    while (c < nb) {
+        const int gn = min(G, nb - c);
+        uint32_t base[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (g >= gn) break;
+            const int sg = st + g < S ? st + g : st + g - S;
+            const uint32_t pg = st + g < S ? parity : parity ^ 1u;
+            if (!mbar_wait_bounded(&full[sg], pg, err)) s_abort = 1;
+            base[g] = ring + (uint32_t)sg * stage_bytes;
+        }
+        __syncthreads();   // every thread has waited (or given up) on the group's stages
+        if (s_abort) break;
+        T *yslice = Y + (b0 + c) * out_slice;
+        for (int y = y0; y < y1; ++y) {
+            uint32_t ry[KY];
+            float wy[KY];
+#pragma unroll
+            for (int k = 0; k < KY; ++k) {
+                ry[k] = s_ry[(y - y0) * KY + k];
+                wy[k] = s_wy[(y - y0) * KY + k];
+            }
+            const bool fy = s_fy[y - y0] != 0;
+            T *yrow = yslice + (int64_t)y * nx + tid;
+#pragma unroll
+            for (int j = 0; j < kRsRowsMaxCols; ++j) {
+                if (j >= ncols) break;
+                const int x = tid + j * kRsThreads;
+                if (x >= nx) break;
+                if (fy || cf[j]) {
+                    for (int g = 0; g < gn; ++g) yrow[g * out_slice + j * kRsThreads] = ext;
+                    continue;
+                }
+                float acc[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    acc[g] = 0.0f;
+                    if (g >= gn) continue;
+#pragma unroll
+                    for (int ky = 0; ky < KY; ++ky) {
+                        const uint32_t row = base[g] + ry[ky];
+                        float sx = 0.0f;
+#pragma unroll
+                        for (int kx = 0; kx < KX; ++kx) sx = fmaf(cw[j][kx], lds_at<T>(row + cx[j][kx]), sx);
+                        acc[g] = fmaf(wy[ky], sx, acc[g]);
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (g < gn) yrow[g * out_slice + j * kRsThreads] = IO<T>::st(acc[g]);
+            }
+        }
+        __syncthreads();   // the group's stages fully read
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            for (int g = 0; g < gn; ++g) {
+                if (c + g + S >= nb) break;
+                const int sg = st + g < S ? st + g : st + g - S;
+                mbar_arrive_expect_tx(&full[sg], stage_bytes);
+                bulk_copy_g2s(rs_smem + (size_t)sg * stage_bytes,
+                              src + (int64_t)(c + g + S) * in_slice, stage_bytes, &full[sg]);
+            }
+        }
+        c += gn;
+        st += gn;
+        if (st >= S) {
+            st -= S;
+            parity ^= 1u;
+        }
+    }
+    if (c < nb && tid == 0) {
+        // a wait gave up: let the copies still in flight land before the
+        // block's shared memory is released (bounded again)
+        for (int cc = c; cc < nb && cc < c + S; ++cc)
+            mbar_wait_bounded(&full[cc % S], (uint32_t)(cc / S) & 1u, nullptr);
+    }
+}
+
+template <typename T, int KY, int KX, int G>
+static cudaError_t launch_stage_g(const T *X, T *Y, const ResizeTables &tb, const ResizeArgs &p,
+                                  dim3 grid, int rows, int per, unsigned *err, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(resize_stage_kernel<T, KY, KX, G>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kRsStageRing);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int H = p.r == 2 ? p.ax[1].n_in : 1, W = p.ax[2].n_in;
+    resize_stage_kernel<T, KY, KX, G><<<grid, kRsThreads, kRsStageRing, s>>>(
+        X, Y, tb, p.B, H, W, rows, per, p.extrapolation_value, err);
+    return cudaGetLastError();
+}
+
+// G: slices per pass, at most half the stages.  Sixteen taps per output
+// (4 x 4) keep G = 1: grouping them spills registers.
+template <typename T, int KY, int KX>
+static cudaError_t launch_stage_kernel(const T *X, T *Y, const ResizeTables &tb,
+                                       const ResizeArgs &p, dim3 grid, int rows, int per,
+                                       int stages, unsigned *err, cudaStream_t s) {
+    if (KY * KX < 16 && stages >= 8)
+        return launch_stage_g<T, KY, KX, (KY * KX < 16 ? 4 : 1)>(X, Y, tb, p, grid, rows, per, err, s);
+    if (KY * KX < 16 && stages >= 4)
+        return launch_stage_g<T, KY, KX, (KY * KX < 16 ? 2 : 1)>(X, Y, tb, p, grid, rows, per, err, s);
+    return launch_stage_g<T, KY, KX, 1>(X, Y, tb, p, grid, rows, per, err, s);
+}
+
+// Staged row kernel when the row kernel's tables apply, rows are whole
+// 16-byte chunks and every band's input rows fit two stages; *used reports
+// whether it ran.
+template <typename T>
+cudaError_t launch_resize_stage(const void *X, void *Y, const ResizeArgs &p, unsigned *err,
+                                cudaStream_t s, bool *used) {
+    *used = false;
+    const int W = p.ax[2].n_in;
+    if (((size_t)W * sizeof(T)) % 16 != 0 || (uintptr_t)X % 16 != 0) return cudaSuccess;
+    ResizeTables tb;
+    if (!build_resize_tables(p, tb)) return cudaSuccess;
+    const int ny = tb.ny, kx = tb.kx, ky = tb.ky;
+    // fp32 with at most four taps per output measured faster on the row
+    // kernel (2x bilinear upscale of 16x64x128x128: 108 us there, 129 us here)
+    if (sizeof(T) == 4 && kx * ky <= 4) return cudaSuccess;
+    const int *yi = reinterpret_cast<const int *>(tb.data + (size_t)tb.nx * kx * 8);
+    const unsigned char *yf = tb.data + ((size_t)tb.nx * kx + (size_t)ny * ky) * 8 + tb.nx;
+    auto max_rows = [&](int th) {
+        int m = 1;
+        for (int y0 = 0; y0 < ny; y0 += th) {
+            int lo = 0x7fffffff, hi = -1;
+            for (int y = y0; y < std::min(ny, y0 + th); ++y) {
+                if (yf[y]) continue;
+                for (int k = 0; k < ky; ++k) {
+                    lo = std::min(lo, yi[y * ky + k]);
+                    hi = std::max(hi, yi[y * ky + k]);
+                }
+            }
+            if (hi >= 0) m = std::max(m, hi - lo + 1);
+        }
+        return m;
+    };
+    // tallest band (up to 32 output rows) whose input rows fit two stages:
+    // every slice costs the block two barriers, so taller bands amortise them
+    int rows = kRsStageRows;
+    while (rows > 1 && (size_t)2 * max_rows(rows) * W * sizeof(T) > (size_t)kRsStageRing) rows >>= 1;
+    const size_t stage = (size_t)max_rows(rows) * W * sizeof(T);
+    if (2 * stage > (size_t)kRsStageRing) return cudaSuccess;
+    const int stages = (int)std::min<size_t>(kRsStageMax, kRsStageRing / stage);
+    // slices per block: several waves of blocks
+    int64_t per = 64;
+    auto blocks = [&](int64_t p_) { return (int64_t)((ny + rows - 1) / rows) * ((p.B + p_ - 1) / p_); };
+    while (per > 1 && blocks(per) < 12 * 152) per >>= 1;
+    per = std::max<int64_t>(per, (p.B + 65534) / 65535);
+    const dim3 grid((unsigned)((ny + rows - 1) / rows), (unsigned)((p.B + per - 1) / per));
+    const T *x = (const T *)X;
+    T *y = (T *)Y;
+    cudaError_t e;
+    const int pb = (int)per;
+    if (kx == 1 && ky == 1) e = launch_stage_kernel<T, 1, 1>(x, y, tb, p, grid, rows, pb, stages, err, s);
+    else if (ky == 1 && kx == 2) e = launch_stage_kernel<T, 1, 2>(x, y, tb, p, grid, rows, pb, stages, err, s);
+    else if (ky == 1 && kx == 4) e = launch_stage_kernel<T, 1, 4>(x, y, tb, p, grid, rows, pb, stages, err, s);
+    else if (kx == 2) e = launch_stage_kernel<T, 2, 2>(x, y, tb, p, grid, rows, pb, stages, err, s);
+    else e = launch_stage_kernel<T, 4, 4>(x, y, tb, p, grid, rows, pb, stages, err, s);
+    *used = true;
+    return e;
 }
 
 template <typename T, int R>
@@ -583,7 +866,9 @@ static cudaError_t launch_resize_r(const void *X, void *Y, const ResizeArgs &p, 
 template <typename T>
 cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &p, cudaStream_t s) {
     bool used = false;
-    const cudaError_t e = launch_resize_rows<T>(X, Y, p, s, &used);
+    cudaError_t e = launch_resize_stage<T>(X, Y, p, p.err, s, &used);
+    if (used || e != cudaSuccess) return e;
+    e = launch_resize_rows<T>(X, Y, p, s, &used);
     if (used || e != cudaSuccess) return e;
     if (p.r == 1) return launch_resize_r<T, 1>(X, Y, p, s);
     if (p.r == 2) return launch_resize_r<T, 2>(X, Y, p, s);

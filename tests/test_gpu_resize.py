@@ -134,6 +134,40 @@ def test_resize_crop_and_extrapolation(gs_cuda, oracle_mod, dtype):
          coordinate_transformation_mode="tf_crop_and_resize")
 
 
+STAGED = [(m, c, dt) for m in ("nearest", "linear", "cubic")
+          for c in COORDS + ["tf_crop_and_resize"] for dt in DTYPES]
+
+
+@pytest.mark.parametrize("mode,coord,dtype", STAGED)
+def test_resize_staged_rows_match_the_row_kernel(gs_cuda, oracle_mod, mode, coord, dtype):
+    """Inputs whose rows are whole 16-byte chunks take the staged row kernel
+    (each slice's input rows bulk-copied into shared memory first); the same
+    input one element off 16-byte alignment takes the plain row kernel.  Both
+    match the oracle, and each other bit for bit."""
+    g = wl.rng(zlib.crc32(repr((mode, coord, dtype, "staged")).encode()))
+    X = g.normal(size=(3, 5, 21, 40))
+    Xt = wl.as_dtype(X, dtype)
+    cases = [dict(scales=_f32([1, 1, 1.7, 2.3])), dict(scales=_f32([1, 1, 0.45, 0.6])),
+             dict(sizes=[3, 5, 63, 16]), dict(scales=_f32([1, 1, 1, 2.0]))]
+    for case in cases:
+        kw = dict(case, mode=mode, coordinate_transformation_mode=coord)
+        if coord == "tf_crop_and_resize":
+            kw.update(roi=_f32([0, 0, -0.2, 0.1, 1, 1, 0.9, 1.3]), extrapolation_value=-3.5)
+        Y1 = gs_cuda.gs_resize(Xt.cuda(), **kw)
+        buf = torch.empty(Xt.numel() + 1, dtype=Xt.dtype, device="cuda")
+        Xu = buf[1:].view(Xt.shape)
+        Xu.copy_(Xt.cuda())
+        Y2 = gs_cuda.gs_resize(Xu, **kw)
+        assert gs_cuda.gs_device_status() == 0
+        what = f"staged {mode} {coord} {dtype} {case}"
+        assert torch.equal(Y1, Y2), what
+        ref = oracle_mod.resize(wl.widened(Xt), **kw)
+        if mode == "nearest":
+            np.testing.assert_array_equal(wl.widened(Y1), ref, err_msg=what)
+        else:
+            assert_parity(Y1, ref, dtype, what)
+
+
 @pytest.mark.parametrize("policy", ["stretch", "not_larger", "not_smaller"])
 def test_resize_keep_aspect_ratio(gs_cuda, oracle_mod, policy):
     X = wl.rng(6).normal(size=(1, 2, 9, 14))
