@@ -219,6 +219,38 @@ gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const 
                            cudaStream_t stream);
 
 /*
+ * gs_affine_sample_from_host -- gs_affine_sample with theta, X and Y in host
+ * memory: the batch is cut into `chunks` runs of whole images, and for each
+ * run the upload of theta and X (streams[0]), the kernel (streams[1]) and the
+ * download of Y (streams[2]) are enqueued with cudaMemcpyAsync and ordered by
+ * events, so the copies of neighbouring runs overlap the kernels.  The
+ * operator is independent per image, so the result equals gs_affine_sample's
+ * bit for bit.
+ *
+ *   theta_h, X_h, Y_h     host; page-locked (cudaHostAlloc / cudaHostRegister)
+ *                         for the copies to overlap, pageable works but
+ *                         serialises them.  Y_h is written.
+ *   theta_d, X_d, Y_d     device buffers of the full sizes (caller-owned; the
+ *                         library allocates nothing), aligned as gs_affine_sample
+ *                         wants X, theta and Y.
+ *   chunks                runs to cut the batch into (clamped to [1, N]).
+ *   streams               host, three caller-owned streams: upload, kernel,
+ *                         download.  Nothing orders them against other work:
+ *                         make streams[0] wait for whatever produced theta_h
+ *                         and X_h, and wait on streams[2] before reading Y_h.
+ *   Other arguments as gs_affine_sample.
+ *
+ * Errors as gs_affine_sample; GS_ERR_NULL for a missing host or device buffer
+ * or stream array; GS_ERR_CUDA if a copy, event or launch fails to enqueue
+ * (runs already enqueued stay enqueued).
+ */
+gs_status gs_affine_sample_from_host(const void *theta_h, const int64_t *size, int r,
+                                     const void *X_h, const int64_t *x_shape, gs_dtype dt,
+                                     gs_mode mode, gs_pad pad, int align_corners,
+                                     float cubic_coeff_a, void *Y_h, void *theta_d, void *X_d,
+                                     void *Y_d, int chunks, const cudaStream_t *streams);
+
+/*
  * DeformConv attributes.  The DeformConv page lists no Attributes section; its
  * examples use kernel_shape, pads and offset_group.  The rest follow ONNX Conv:
  *   kernel     (kH, kW); 0 means "take it from W".

@@ -552,6 +552,71 @@ gs_status gs_affine_sample(const void *theta, const int64_t *size, int r, const 
     });
 }
 
+gs_status gs_affine_sample_from_host(const void *theta_h, const int64_t *size, int r,
+                                     const void *X_h, const int64_t *x_shape, gs_dtype dt,
+                                     gs_mode mode, gs_pad pad, int align_corners,
+                                     float cubic_coeff_a, void *Y_h, void *theta_d, void *X_d,
+                                     void *Y_d, int chunks, const cudaStream_t *streams) {
+    if (r != 2 && r != 3) return GS_ERR_RANK;
+    if (!size || !x_shape) return GS_ERR_NULL;
+    if (size[0] != x_shape[0] || size[1] != x_shape[1]) return GS_ERR_SHAPE;
+    gs::SampleArgs args;
+    bool skip = false;
+    gs_status st = check_sample(X_d, x_shape, r, size + 2, dt, mode, pad, align_corners,
+                                cubic_coeff_a, Y_d, &args, &skip);
+    if (st != GS_OK || skip) return st;
+    if (!theta_d || !theta_h || !X_h || !Y_h || !streams) return GS_ERR_NULL;
+    if (!aligned(theta_d, elem_size(dt))) return GS_ERR_ALIGN;
+    args.err = error_word();
+    const int64_t N = args.N;
+    const int64_t runs = chunks < 1 ? 1 : (chunks > N ? N : chunks);
+    const int64_t step = (N + runs - 1) / runs;
+    const size_t es = elem_size(dt);
+    const size_t th_img = (size_t)r * (r + 1) * es;
+    const size_t x_img = (size_t)args.C * (size_t)args.in_plane * es;
+    const size_t y_img = (size_t)args.C * (size_t)args.out_plane * es;
+    cudaEvent_t ev_in = nullptr, ev_run = nullptr;
+    if (cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev_run, cudaEventDisableTiming) != cudaSuccess) {
+        if (ev_in) cudaEventDestroy(ev_in);
+        return GS_ERR_CUDA;
+    }
+    const cudaStream_t s_in = streams[0], s_run = streams[1], s_out = streams[2];
+    gs_status res = GS_OK;
+    for (int64_t n0 = 0; n0 < N && res == GS_OK; n0 += step) {
+        const int64_t n = N - n0 < step ? N - n0 : step;
+        const char *th_src = static_cast<const char *>(theta_h) + n0 * th_img;
+        const char *x_src = static_cast<const char *>(X_h) + n0 * x_img;
+        char *th_dst = static_cast<char *>(theta_d) + n0 * th_img;
+        char *x_dst = static_cast<char *>(X_d) + n0 * x_img;
+        char *y_dev = static_cast<char *>(Y_d) + n0 * y_img;
+        char *y_dst = static_cast<char *>(Y_h) + n0 * y_img;
+        // the event calls order the streams: a wait enqueued here refers to the
+        // record just before it, so both events are reused run after run
+        if (cudaMemcpyAsync(th_dst, th_src, n * th_img, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(x_dst, x_src, n * x_img, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+            cudaEventRecord(ev_in, s_in) != cudaSuccess ||
+            cudaStreamWaitEvent(s_run, ev_in, 0) != cudaSuccess) {
+            res = GS_ERR_CUDA;
+            break;
+        }
+        gs::SampleArgs a = args;
+        a.N = (int)n;
+        const gs_status ls = dispatch(dt, [&](auto tag) {
+            return gs::launch_sample<decltype(tag)>(x_dst, th_dst, y_dev, a, r, (int)mode, true,
+                                                    nullptr, 0, s_run);
+        });
+        if (ls != GS_OK || cudaEventRecord(ev_run, s_run) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, ev_run, 0) != cudaSuccess ||
+            cudaMemcpyAsync(y_dst, y_dev, n * y_img, cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
+            res = GS_ERR_CUDA;
+    }
+    // events may be destroyed with work still pending on them
+    cudaEventDestroy(ev_in);
+    cudaEventDestroy(ev_run);
+    return res;
+}
+
 gs_status gs_deform_conv(const void *X, const int64_t *x_shape, const void *W, int64_t oC,
                          const void *offset, const void *B, const void *mask,
                          const gs_deform_attrs *at, gs_dtype dt, void *Y, cudaStream_t stream) {

@@ -95,6 +95,25 @@ def test_ranks_four_to_six_are_accepted(L, r, entry):
     assert _gsample(L, [2, 3] + [4] * (r - 1) + [-1], [3] * r, r=r, entry=entry) == 3
 
 
+def test_affine_sample_from_host_checks(L):
+    f = L.gs_affine_sample_from_host
+    streams = (ctypes.c_void_p * 3)(None, None, None)
+    size, xs = _i64([2, 3, 4, 4]), _i64([2, 3, 4, 4])
+
+    def call(r=2, size=size, xs=xs, theta_h=FAKE, X_h=FAKE, Y_h=FAKE, theta_d=FAKE, X_d=FAKE,
+             Y_d=FAKE, streams=streams):
+        return f(theta_h, size, r, X_h, xs, 0, 0, 0, 0, -0.75, Y_h, theta_d, X_d, Y_d, 2, streams)
+
+    assert call(r=1) == 2 and call(r=4) == 2                                  # rank
+    assert call(size=_i64([2, 4, 4, 4])) == 3                                  # C mismatch
+    assert call(streams=None) == 1 and call(X_h=None) == 1 and call(theta_d=None) == 1
+    assert call(Y_d=None) == 1 and call(Y_h=None) == 1
+    assert call(X_d=FAKE + 2) == 6                                             # misaligned
+    # an empty batch returns before any pointer is needed
+    assert call(size=_i64([0, 3, 4, 4]), xs=_i64([0, 3, 4, 4]), theta_h=None, X_h=None, Y_h=None,
+                theta_d=None, X_d=None, Y_d=None, streams=None) == 0
+
+
 def test_static_scratch_rejects_an_image_slot_beyond_its_size(L):
     # (512*513 + 1) * 64 fp32 elements exceed the 64 MiB scratch: refused on the host
     assert _gsample(L, [1, 64, 512, 513], [4, 4], entry="gs_grid_sample_static") == 3
