@@ -4,7 +4,7 @@ Sampling shards by image with no exchange step, so a run on N GPUs is N
 independent replicas.  Each rank draws its own images (the workload's seed +
 rank) and times its own replica; the job's time is the slowest rank's, and the
 job's throughput counts every rank's outputs.  The one collective is the
-max over ranks of the timings.  On a GPU box that collective runs on NCCL;
+max over ranks of the timings.  With GPUs that collective runs on NCCL;
 here the same helpers run on gloo, and the launcher path (torchrun, rank 0
 prints the line, the other ranks print nothing) runs end to end through the
 reference arm, which needs no GPU.
