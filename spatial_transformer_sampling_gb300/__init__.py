@@ -109,12 +109,14 @@ def load_library(path=None):
     L.gs_status_str.argtypes = [ci]
     L.gs_status_str.restype = ctypes.c_char_p
     L.gs_device_status.argtypes = [vp]
+    L.gs_test_bounded_wait_expires.argtypes = [ctypes.c_uint64, vp]
     L.gs_version.restype = ctypes.c_char_p
     for f in ("gs_affine_grid", "gs_grid_sample", "gs_grid_sample_workspace_size",
               "gs_grid_sample_ws", "gs_grid_sample_static", "gs_affine_sample",
               "gs_affine_sample_from_host", "gs_deform_conv",
               "gs_deform_conv_workspace_size", "gs_deform_conv_ws", "gs_device_status",
-              "gs_resize_output_shape", "gs_resize", "gs_grid_sample_int"):
+              "gs_resize_output_shape", "gs_resize", "gs_grid_sample_int",
+              "gs_test_bounded_wait_expires"):
         getattr(L, f).restype = ci
     if path is None:
         _lib = L
@@ -152,6 +154,26 @@ def _check_tensors(*ts):
     return ref
 
 
+def _shape_error(what, got, want):
+    raise ValueError(f"{what} has shape {tuple(got)}, expected {tuple(want)}")
+
+
+def _check_sample_shapes(X, grid, out):
+    """The C ABI receives X's shape and the output extents only, and trusts that
+    grid is (N, out..., r) and out is (N, C, out...): check both here.  Shapes
+    only, so that it runs before (and without) any device work."""
+    if X.dim() < 3:
+        raise ValueError(f"X must be (N, C, spatial...), got {tuple(X.shape)}")
+    r = X.dim() - 2
+    if grid.dim() != X.dim() or grid.shape[0] != X.shape[0] or grid.shape[-1] != r:
+        raise ValueError(f"grid has shape {tuple(grid.shape)}, expected (N={X.shape[0]}, "
+                         f"{r} output extents, {r}) for X of shape {tuple(X.shape)}")
+    want = list(X.shape[:2]) + list(grid.shape[1:-1])
+    if out is not None and list(out.shape) != want:
+        _shape_error("out", out.shape, want)
+    return r, list(grid.shape[1:-1])
+
+
 def _i64(vals):
     arr = (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
     return arr
@@ -173,9 +195,13 @@ def _ok(status, where):
 def gs_affine_grid(theta, size, align_corners=0, out=None):
     """AffineGrid: theta (N, r, r+1) -> grid (N, spatial..., r); size = (N, C, spatial...)."""
     torch = _torch()
-    _check_tensors(theta, out)
     size = [int(s) for s in size]
     r = len(size) - 2
+    if list(theta.shape) != [size[0], r, r + 1]:
+        _shape_error("theta", theta.shape, (size[0], r, r + 1))
+    if out is not None and list(out.shape) != [size[0]] + size[2:] + [r]:
+        _shape_error("out", out.shape, [size[0]] + size[2:] + [r])
+    _check_tensors(theta, out)
     if out is None:
         out = torch.empty([size[0]] + size[2:] + [r], dtype=theta.dtype, device=theta.device)
     _ok(load_library().gs_affine_grid(_ptr(theta), _dtype_code(theta), r, _i64(size),
@@ -192,9 +218,8 @@ def gs_grid_sample(X, grid, mode="linear", padding_mode="zeros", align_corners=0
     raw bytes) or "auto" (one of the size gs_grid_sample_workspace_size asks
     for, from torch's allocator) calls gs_grid_sample_ws."""
     torch = _torch()
+    r, out_sp = _check_sample_shapes(X, grid, out)
     _check_tensors(X, grid, out)
-    r = X.dim() - 2
-    out_sp = list(grid.shape[1:-1])
     if out is None:
         out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
     if workspace is not None:
@@ -222,11 +247,12 @@ def gs_grid_sample_int(X, grid, mode="linear", padding_mode="zeros", align_corne
     """GridSample with an integer X (uint8, int8, uint16, int16) and a float grid: fp32
     intermediates, truncated toward zero and saturated at the end (gs_grid_sample_int)."""
     torch = _torch()
+    r, out_sp = _check_sample_shapes(X, grid, out)
     for t in (X, grid, out):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("libgs takes contiguous CUDA tensors")
-    r = X.dim() - 2
-    out_sp = list(grid.shape[1:-1])
+    if out is not None and out.dtype != X.dtype:
+        raise ValueError("out must have X's dtype")
     if out is None:
         out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
     _ok(load_library().gs_grid_sample_int(_ptr(X), _int_code(X), _i64(X.shape), r, _ptr(grid),
@@ -252,9 +278,8 @@ def gs_grid_sample_ws(X, grid, workspace="auto", mode="linear", padding_mode="ze
                       align_corners=0, cubic_coeff_a=-0.75, out=None):
     """gs_grid_sample with a device workspace (see gs_grid_sample_ws in gs.h)."""
     torch = _torch()
+    r, out_sp = _check_sample_shapes(X, grid, out)
     _check_tensors(X, grid, out)
-    r = X.dim() - 2
-    out_sp = list(grid.shape[1:-1])
     if out is None:
         out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
     if isinstance(workspace, str):
@@ -283,9 +308,8 @@ def gs_grid_sample_static(X, grid, mode="linear", padding_mode="zeros", align_co
     this wrapper from allocating the output with torch.  Concurrent calls race on
     the one scratch; the first call on a device should precede any stream capture."""
     torch = _torch()
+    r, out_sp = _check_sample_shapes(X, grid, out)
     _check_tensors(X, grid, out)
-    r = X.dim() - 2
-    out_sp = list(grid.shape[1:-1])
     if out is None:
         out = torch.empty(list(X.shape[:2]) + out_sp, dtype=X.dtype, device=X.device)
     _ok(load_library().gs_grid_sample_static(_ptr(X), _i64(X.shape), r, _ptr(grid),
@@ -303,9 +327,16 @@ def gs_affine_sample(theta, size, X, mode="linear", padding_mode="zeros", align_
                      cubic_coeff_a=-0.75, out=None):
     """GridSample(X, AffineGrid(theta, size)) in one kernel; size = (N, C, out...)."""
     torch = _torch()
-    _check_tensors(X, theta, out)
     size = [int(s) for s in size]
     r = X.dim() - 2
+    if len(size) != X.dim() or size[:2] != list(X.shape[:2]):
+        raise ValueError(f"size {tuple(size)} must be (N, C, out...) with X's N and C "
+                         f"(X has shape {tuple(X.shape)})")
+    if list(theta.shape) != [size[0], r, r + 1]:
+        _shape_error("theta", theta.shape, (size[0], r, r + 1))
+    if out is not None and list(out.shape) != size:
+        _shape_error("out", out.shape, size)
+    _check_tensors(X, theta, out)
     if out is None:
         out = torch.empty(list(X.shape[:2]) + size[2:], dtype=X.dtype, device=X.device)
     _ok(load_library().gs_affine_sample(_ptr(theta), _i64(size), r, _ptr(X), _i64(X.shape),
@@ -332,6 +363,30 @@ def deform_out_hw(H, W, a):
     return oH, oW
 
 
+def _check_deform_shapes(X, W, offset, B, mask, out, a, oH, oW):
+    """The C ABI receives X's shape, oC and the attributes only, and trusts the
+    other tensors' shapes: check them here (shapes only, no device work)."""
+    N, C = X.shape[0], X.shape[1]
+    oC = W.shape[0]
+    K = int(a.kernel[0]) * int(a.kernel[1])
+    og, grp = int(a.offset_group), int(a.group)
+    if grp < 1 or C % grp:
+        raise ValueError(f"group {grp} does not divide C = {C}")
+    want_w = (oC, C // grp, int(a.kernel[0]), int(a.kernel[1]))
+    if tuple(W.shape) != want_w:
+        _shape_error("W", W.shape, want_w)
+    if oH < 1 or oW < 1:
+        return   # the library rejects or skips these before touching memory
+    if tuple(offset.shape) != (N, og * K * 2, oH, oW):
+        _shape_error("offset", offset.shape, (N, og * K * 2, oH, oW))
+    if B is not None and tuple(B.shape) != (oC,):
+        _shape_error("B", B.shape, (oC,))
+    if mask is not None and tuple(mask.shape) != (N, og * K, oH, oW):
+        _shape_error("mask", mask.shape, (N, og * K, oH, oW))
+    if out is not None and tuple(out.shape) != (N, oC, oH, oW):
+        _shape_error("out", out.shape, (N, oC, oH, oW))
+
+
 def gs_deform_conv(X, W, offset, B=None, mask=None, kernel_shape=None, pads=None, strides=None,
                    dilations=None, group=1, offset_group=1, out=None, workspace=None):
     """DeformConv 2-D: X (N,C,H,W), W (oC,C/group,kH,kW), offset (N,og*kH*kW*2,oH,oW).
@@ -340,10 +395,13 @@ def gs_deform_conv(X, W, offset, B=None, mask=None, kernel_shape=None, pads=None
     "auto" (the size gs_deform_conv_workspace_size asks for, from torch's
     allocator) calls gs_deform_conv_ws."""
     torch = _torch()
-    _check_tensors(X, W, offset, B, mask, out)
+    if X.dim() != 4 or W.dim() != 4:
+        raise ValueError(f"X and W must be 4-D, got {tuple(X.shape)} and {tuple(W.shape)}")
     a = deform_attrs(kernel_shape if kernel_shape is not None else W.shape[2:], pads, strides,
                      dilations, group, offset_group)
     oH, oW = deform_out_hw(X.shape[2], X.shape[3], a)
+    _check_deform_shapes(X, W, offset, B, mask, out, a, oH, oW)
+    _check_tensors(X, W, offset, B, mask, out)
     if out is None:
         out = torch.empty((X.shape[0], W.shape[0], oH, oW), dtype=X.dtype, device=X.device)
     L = load_library()

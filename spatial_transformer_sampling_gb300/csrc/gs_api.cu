@@ -7,6 +7,7 @@
 
 #include "../../include/gs.h"
 #include "gs_internal.h"
+#include "gs_ptx.cuh"
 
 // Device error word: kernels whose bounded waits give up record it here;
 // gs_device_status reads and clears it.
@@ -18,34 +19,49 @@ __device__ unsigned g_gs_error_word = 0;
 // sampler then reads, the zero pixels included.
 static __device__ __align__(256) unsigned char g_gs_static_ws[GS_STATIC_WORKSPACE_BYTES];
 
-namespace {
-
-// Device address of g_gs_error_word on the current device (looked up once per
-// device; a host-side symbol is not a device address).
-unsigned *error_word() {
-    static unsigned *cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_gs_error_word) != cudaSuccess) return nullptr;
-        cache[dev] = (unsigned *)p;
-    }
-    return cache[dev];
+// Test hook behind gs_test_bounded_wait_expires: one thread arms an mbarrier
+// for 16 bytes of transfer that no copy will ever deliver (none is issued), so
+// the phase cannot complete, and waits on it with the pipelines' bounded wait.
+// The wait gives up after limit_ns, sets the timeout bit in the error word and
+// the kernel returns; nothing is in flight, so leaving is safe.
+__global__ void bounded_wait_probe_kernel(unsigned *err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    gs::mbar_init(&bar, 1);
+    gs::fence_mbar_init();
+    gs::mbar_arrive_expect_tx(&bar, 16);
+    gs::mbar_wait_bounded(&bar, 0, err, limit_ns);
+    gs::mbar_inval(&bar);
 }
 
-// Device address of g_gs_static_ws on the current device, looked up once per
-// device (nullptr if the lookup fails).
-void *static_workspace() {
-    static void *cache[64] = {};
+namespace {
+
+// Device address of a __device__ symbol on the current device, looked up once
+// per device (a host-side symbol is not a device address; nullptr if the
+// lookup fails).  The per-device caches are atomics: first calls from several
+// host threads may both look the address up, and both store the same value.
+template <typename S>
+void *symbol_address(std::atomic<void *> (&cache)[gs::kMaxDevices], const S &symbol) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_gs_static_ws) != cudaSuccess) return nullptr;
-        cache[dev] = p;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gs::kMaxDevices) return nullptr;
+    void *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+        cache[dev].store(p, std::memory_order_release);
     }
-    return cache[dev];
+    return p;
+}
+
+// Device address of g_gs_error_word.
+unsigned *error_word() {
+    static std::atomic<void *> cache[gs::kMaxDevices];
+    return (unsigned *)symbol_address(cache, g_gs_error_word);
+}
+
+// Device address of g_gs_static_ws.
+void *static_workspace() {
+    static std::atomic<void *> cache[gs::kMaxDevices];
+    return symbol_address(cache, g_gs_static_ws);
 }
 
 constexpr int64_t kMaxExtent = int64_t(1) << 20;
@@ -694,6 +710,14 @@ gs_status gs_device_status(cudaStream_t stream) {
     return GS_OK;
 }
 
-const char *gs_version(void) { return "0.1.0"; }
+gs_status gs_test_bounded_wait_expires(uint64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return GS_ERR_ATTR;
+    unsigned *err = error_word();
+    if (!err) return GS_ERR_CUDA;
+    bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? GS_OK : GS_ERR_CUDA;
+}
+
+const char *gs_version(void) { return "0.2.0"; }
 
 }  // extern "C"

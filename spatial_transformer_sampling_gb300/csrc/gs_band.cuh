@@ -420,15 +420,11 @@ cudaError_t launch_band(const void *X, const void *theta, void *Y, const SampleP
                        (kPairs == kPairAdjacent && Wo % 2 == 0 &&
                         (uintptr_t)Y % (2 * sizeof(T)) == 0);
     auto kern = pairs ? band_kernel<T, MODE, kPairs> : band_kernel<T, MODE, kPairNone>;
-    static bool attr_set[2][64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[pairs][dev]) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[pairs][dev] = true;
-    }
+    static DeviceFlags attr_set[2];
+    const cudaError_t e = once_per_device(attr_set[pairs], [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    });
+    if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((int64_t)a.N * B.bands);
     kern<<<blocks, kBandThreads, kRingBytes, s>>>((const T *)X, (const T *)theta, (T *)Y, P, B);
     *used = true;

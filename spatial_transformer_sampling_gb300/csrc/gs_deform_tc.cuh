@@ -611,10 +611,8 @@ cudaError_t launch_deform_tc_ws(const void *X, const void *W, const void *offset
     if (ws_bytes < wreg + slot) return cudaSuccess;
     // the largest dynamic shared memory this path uses (deform_tc_params), set
     // once per device
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    static DeviceFlags attr_set;
+    const cudaError_t ae = once_per_device(attr_set, [] {
         for (const void *f : {(const void *)deform_tc_nhwc_kernel<T, 64>,
                               (const void *)deform_tc_nhwc_kernel<T, 32>,
                               (const void *)deform_tc_nhwc_kernel<T, 16>}) {
@@ -622,8 +620,9 @@ cudaError_t launch_deform_tc_ws(const void *X, const void *W, const void *offset
                 cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
             if (e != cudaSuccess) return e;
         }
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+        return cudaSuccess;
+    });
+    if (ae != cudaSuccess) return ae;
     const int K = a.kH * a.kW;
     const int packs = K * a.oC * (a.C / 8);
     uint16_t *slots = (uint16_t *)((unsigned char *)ws + wreg);

@@ -5,7 +5,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gs {
+
+// Host-side per-device setup (a kernel's shared-memory attribute, a symbol's
+// device address) runs on the first call that needs it on each device.  The
+// flags are atomics, so first calls from several host threads at once do not
+// race on them; the setup steps are idempotent, so two such calls may both run
+// a step and both get the same result.
+constexpr int kMaxDevices = 64;
+
+struct DeviceFlags {
+    std::atomic<bool> set[kMaxDevices];
+};
+
+// Runs setup() unless it already succeeded on the current device; returns its
+// error (cudaSuccess once done).
+template <typename F>
+cudaError_t once_per_device(DeviceFlags &flags, F &&setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached && flags.set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess && cached) flags.set[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 constexpr int kSampleThreads = 256;
 

@@ -60,18 +60,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with `parity` to complete; gives up after kWaitLimitNs,
-// records kDevErrTimeout in *err and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err) {
+// Waits for the phase with `parity` to complete; gives up after `limit_ns`
+// (default kWaitLimitNs), records kDevErrTimeout in *err and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             if (err) atomicOr(err, kDevErrTimeout);
             return false;
         }
     }
     return true;
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Bulk asynchronous copy of `bytes` (a multiple of 16; both addresses 16-byte

@@ -201,7 +201,7 @@ template <typename T, int R, int K>
 __global__ void __launch_bounds__(kRsThreads)
 resize_kernel(const T *__restrict__ X, T *__restrict__ Y, const ResizeArgs p, const ResizeTile tl,
               int slices_per_block) {
-    extern __shared__ __align__(16) unsigned char rs_smem[];
+    extern __shared__ __align__(128) unsigned char rs_smem[];
     const int tid = threadIdx.x;
     int tile = blockIdx.x;
     int tc[3];
@@ -738,16 +738,12 @@ resize_stage_kernel(const T *__restrict__ X, T *__restrict__ Y,
 template <typename T, int KY, int KX, int G>
 static cudaError_t launch_stage_g(const T *X, T *Y, const ResizeTables &tb, const ResizeArgs &p,
                                   dim3 grid, int rows, int per, unsigned *err, cudaStream_t s) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(resize_stage_kernel<T, KY, KX, G>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kRsStageRing);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    static DeviceFlags attr_set;
+    const cudaError_t e = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(resize_stage_kernel<T, KY, KX, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kRsStageRing);
+    });
+    if (e != cudaSuccess) return e;
     const int H = p.r == 2 ? p.ax[1].n_in : 1, W = p.ax[2].n_in;
     resize_stage_kernel<T, KY, KX, G><<<grid, kRsThreads, kRsStageRing, s>>>(
         X, Y, tb, p.B, H, W, rows, per, p.extrapolation_value, err);

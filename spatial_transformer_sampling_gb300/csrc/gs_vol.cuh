@@ -370,15 +370,12 @@ cudaError_t launch_vol(const void *X, const void *theta, void *Y, const SamplePa
     const int64_t tiles = (int64_t)((Do + V.tz - 1) / V.tz) * V.tiles_y * V.tiles_x;
     if (tiles * a.N > 0x7fffffffLL) return cudaSuccess;
     V.tiles = (int)tiles;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            vol_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVolSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    static DeviceFlags attr_set;
+    const cudaError_t e = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(vol_kernel<T, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kVolSmemBytes);
+    });
+    if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)(tiles * a.N);
     vol_kernel<T, MODE><<<blocks, kVolThreads, kVolSmemBytes, s>>>(
         (const T *)X, (const T *)theta, (T *)Y, P, V);

@@ -251,3 +251,9 @@ def test_integer_x_entry_rejects_bad_types_on_the_host(L):
     # empty output: no launch, no pointers needed
     assert L.gs_grid_sample_int(None, 16, xs, 2, None, 0, _i64([0, 3]), 0, 0, 0, -0.75, None,
                                 None) == 0
+
+
+def test_bounded_wait_hook_rejects_limits_on_the_host(L):
+    # 0 and more than a second are refused before anything is enqueued
+    assert L.gs_test_bounded_wait_expires(0, None) == 5
+    assert L.gs_test_bounded_wait_expires(1_000_000_001, None) == 5

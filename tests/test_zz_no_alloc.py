@@ -69,6 +69,34 @@ def test_static_chunks_a_batch_larger_than_the_scratch(gs_cuda):
         assert torch.equal(Ys, gs_cuda.gs_grid_sample(Xd, Gd, mode, "reflection", 0))
 
 
+# The edges of the chunking over the 64 MiB scratch: one image per chunk with a
+# slot just under the limit, and a batch whose last chunk is exactly full.
+CHUNK_EDGES = [
+    # x_shape, slot bytes / images per chunk
+    ((2, 64, 511, 511), "(511*511 + 1) * 64 * 4 B = 63.75 MiB: one image per chunk, two chunks"),
+    ((6, 256, 128, 128), "16.8 MB slots, three per chunk: two full chunks"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CHUNK_EDGES)))
+def test_static_chunk_edges_match_grid_sample_and_the_oracle(gs_cuda, oracle_mod, case):
+    xs, why = CHUNK_EDGES[case]
+    Xt, Gt = _inputs(970 + case, xs, (24, 20), "float32")
+    Xd, Gd = Xt.cuda(), Gt.cuda()
+    Ys = gs_cuda.gs_grid_sample_static(Xd, Gd, "cubic", "border", 0)
+    assert torch.equal(Ys, gs_cuda.gs_grid_sample(Xd, Gd, "cubic", "border", 0)), why
+    assert gs_cuda.gs_device_status() == 0
+    # a few outputs of every image (first and last channel included) from the oracle
+    g = wl.rng(980 + case)
+    per_img = Ys[0].numel()
+    idx = np.concatenate([n * per_img + np.concatenate([[0, per_img - 1],
+                                                        g.integers(0, per_img, 30)])
+                          for n in range(xs[0])])
+    ref = oracle_mod.grid_sample_at(wl.widened(Xt), wl.widened(Gt), idx, "cubic", "border", 0)
+    got = Ys.reshape(-1)[torch.from_numpy(idx).cuda()]
+    assert_parity(got, ref, "float32", f"static scratch chunk edge: {why}")
+
+
 def test_static_rejects_an_image_larger_than_the_scratch(gs_cuda):
     # (512*513 + 1) * 64 fp32 elements: 67.2 MB > GS_STATIC_WORKSPACE_BYTES
     X = torch.zeros((1, 64, 512, 513), device="cuda")
