@@ -182,9 +182,12 @@ template <typename T>
 cudaError_t launch_deform(const void *X, const void *W, const void *offset, const void *B,
                           const void *mask, void *Y, const DeformArgs &a, cudaStream_t s) {
     if constexpr (!std::is_same<T, float>::value) {
-        // half types: contraction on the tensor cores where the shape allows
+        // half types: contraction on the tensor cores where the shape allows,
+        // on the staged persistent kernel first
         bool used = false;
-        const cudaError_t e = launch_deform_tc<T>(X, W, offset, B, mask, Y, a, s, &used);
+        cudaError_t e = launch_deform_staged<T>(X, W, offset, B, mask, Y, a, s, &used);
+        if (used || e != cudaSuccess) return e;
+        e = launch_deform_tc<T>(X, W, offset, B, mask, Y, a, s, &used);
         if (used || e != cudaSuccess) return e;
     }
     const int P = a.oH * a.oW;
@@ -203,16 +206,26 @@ cudaError_t launch_deform_ws(const void *X, const void *W, const void *offset, c
                              const void *mask, void *Y, const DeformArgs &a, void *ws,
                              size_t ws_bytes, cudaStream_t s) {
     if constexpr (!std::is_same<T, float>::value) {
-        bool used = false;
-        const cudaError_t e = launch_deform_tc_ws<T>(X, W, offset, B, mask, Y, a, ws, ws_bytes, s,
-                                                     &used);
-        if (used || e != cudaSuccess) return e;
+        // the staged kernel needs no workspace: it runs whenever it takes the
+        // call, as in launch_deform
+        if (!deform_staged_takes(a, X, W, offset, mask)) {
+            bool used = false;
+            const cudaError_t e = launch_deform_tc_ws<T>(X, W, offset, B, mask, Y, a, ws, ws_bytes,
+                                                         s, &used);
+            if (used || e != cudaSuccess) return e;
+        }
     }
     return launch_deform<T>(X, W, offset, B, mask, Y, a, s);
 }
 
+// Workspace bytes gs_deform_conv_ws asks for: 0 for shapes the staged kernel
+// takes (given 16-byte aligned tensors), else the channel-last path's.
 template <typename T>
 size_t deform_ws_bytes(const DeformArgs &a) {
+    if (std::is_same<T, float>::value) return 0;
+    const void *aligned16 = reinterpret_cast<const void *>(uintptr_t(256));
+    if (deform_staged_takes(a, aligned16, aligned16, aligned16, a.has_mask ? aligned16 : nullptr))
+        return 0;
     return deform_workspace_bytes<T>(a);
 }
 

@@ -129,6 +129,15 @@ cudaError_t launch_deform_ws(const void *X, const void *W, const void *offset, c
                              size_t ws_bytes, cudaStream_t s);
 template <typename T>
 size_t deform_ws_bytes(const DeformArgs &args);
+// DeformConv (fp16 / bf16) on the staged persistent tensor-core kernel
+// (gs_deform_st.cuh) when it takes the shape and pointers; *used reports
+// whether it ran.  deform_staged_takes answers the same question.
+template <typename T>
+cudaError_t launch_deform_staged(const void *X, const void *W, const void *offset, const void *B,
+                                 const void *mask, void *Y, const DeformArgs &args, cudaStream_t s,
+                                 bool *used);
+bool deform_staged_takes(const DeformArgs &args, const void *X, const void *W, const void *offset,
+                         const void *mask);
 template <typename T>
 cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &args, cudaStream_t s);
 // GridSample with integer X (TX: uint8_t, int8_t, uint16_t, int16_t) and a float

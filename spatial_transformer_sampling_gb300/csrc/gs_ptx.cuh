@@ -116,23 +116,13 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
     }
 }
 
-// Packed fp32 pairs (Blackwell): lane-wise a*b and a*b+c, each rounded to
-// nearest exactly as fmulf / fmaf would round it.
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)));
-    return *reinterpret_cast<float2 *>(&d);
-}
+// Packed fp32 pairs (Blackwell FMUL2 / FFMA2 through the CUDA builtins, so the
+// compiler allocates the register pairs itself): lane-wise a*b and a*b+c, each
+// rounded to nearest exactly as fmulf / fmaf would round it.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
-          "l"(*reinterpret_cast<uint64_t *>(&c)));
-    return *reinterpret_cast<float2 *>(&d);
+    return __ffma2_rn(a, b, c);
 }
 
 }  // namespace gs

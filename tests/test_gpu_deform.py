@@ -213,3 +213,80 @@ def test_full_size_deform2d_workspace(gs_cuda, oracle_mod):
                                     exact(host["B"]), exact(host["mask"]), **kw)
     assert_parity(Y.reshape(-1)[torch.from_numpy(idx).cuda()], ref, "bfloat16",
                   "deform2d with workspace, sampled")
+
+
+# ---------------------------------- staged persistent tensor-core kernel
+#
+# Shapes the staged kernel takes (group = offset_group = 1, C % 16 == 0,
+# W % 8 == 0, oH*oW % 8 == 0, kH*kW in {1, 2, 3, 4, 6, 9}): one or several
+# 16-channel chunks, tiles spanning 1 to 4 output rows and a ragged last tile,
+# stride and dilation, no bias / no mask, large offsets whose taps leave the
+# staged window (read from global memory), and enough tiles that CTAs take
+# more than one.
+STAGED_CASES = [
+    # N, C, H, W, oC, kernel, pads, strides, dilations, bias, mask, offset sigma
+    (2, 64, 24, 32, 64, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True, 1.0),   # 4 rows per tile
+    (1, 16, 10, 128, 16, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True, 1.0),  # 1 row per tile
+    (1, 48, 20, 40, 48, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), False, True, 1.0),  # ragged last tile
+    (2, 32, 16, 16, 32, (1, 1), (0, 0, 0, 0), (1, 1), (1, 1), True, False, 1.0),  # K = 1
+    (1, 32, 33, 48, 16, (2, 2), (1, 0, 0, 1), (2, 2), (2, 1), True, True, 1.0),   # K = 4, stride, dil
+    (1, 16, 20, 24, 256, (3, 2), (1, 1, 1, 0), (1, 2), (1, 1), True, True, 1.0),  # K = 6, oC = 256
+    (2, 32, 32, 32, 32, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True, 6.0),   # taps leave the window
+    (10, 16, 64, 64, 16, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), True, True, 1.0),  # 320 tiles
+    (1, 16, 8, 8, 32, (1, 3), (0, 1, 0, 1), (1, 1), (1, 1), False, False, 0.7),   # K = 3, one tile
+    (1, 32, 12, 16, 16, (2, 1), (0, 0, 1, 0), (1, 1), (1, 1), True, True, 1.0),   # K = 2
+]
+
+
+def _staged_inputs(case, dtype, seed):
+    N, C, H, W, oC, k, p, s, d, has_b, has_m, sig = STAGED_CASES[case]
+    g = wl.rng(seed)
+    oH = (H + p[0] + p[2] - d[0] * (k[0] - 1) - 1) // s[0] + 1
+    oW = (W + p[1] + p[3] - d[1] * (k[1] - 1) - 1) // s[1] + 1
+    K = k[0] * k[1]
+    host = {
+        "X": wl.as_dtype(g.normal(size=(N, C, H, W)), dtype),
+        "W": wl.as_dtype(g.normal(0, 0.05, size=(oC, C) + k), dtype),
+        "offset": wl.as_dtype(g.normal(0, sig, size=(N, K * 2, oH, oW)), dtype),
+        "B": wl.as_dtype(g.normal(size=(oC,)), dtype) if has_b else None,
+        "mask": wl.as_dtype(1.0 / (1.0 + np.exp(-g.normal(size=(N, K, oH, oW)))), dtype)
+        if has_m else None,
+    }
+    return host, dict(kernel_shape=k, pads=p, strides=s, dilations=d)
+
+
+@pytest.mark.parametrize("case,dtype", list(itertools.product(range(len(STAGED_CASES)),
+                                                              ["float16", "bfloat16"])))
+def test_deform_conv_staged_shapes(gs_cuda, oracle_mod, case, dtype):
+    host, kw = _staged_inputs(case, dtype, 800 + case)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    args = (cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"])
+    a = gs_cuda.deform_attrs(kw["kernel_shape"], kw["pads"], kw["strides"], kw["dilations"])
+    # the staged kernel takes these shapes and needs no workspace
+    assert gs_cuda.gs_deform_conv_workspace_size(host["X"].shape, host["W"].shape[0], a,
+                                                 getattr(torch, dtype)) == 0
+    Y = gs_cuda.gs_deform_conv(*args, **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Y, ref, dtype, f"deform staged case {case} {dtype}")
+    # the same call twice gives the same bits, and so does the workspace entry
+    assert torch.equal(Y, gs_cuda.gs_deform_conv(*args, **kw))
+    assert torch.equal(Y, gs_cuda.gs_deform_conv(*args, workspace="auto", **kw))
+
+
+def test_deform_conv_staged_matches_unaligned_fallback(gs_cuda, oracle_mod):
+    """A tensor off the 16-byte alignment the staged kernel wants runs the
+    previous tensor-core kernel; both agree with the oracle."""
+    host, kw = _staged_inputs(0, "bfloat16", 850)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    buf = torch.empty(cu["X"].numel() + 1, dtype=torch.bfloat16, device="cuda")
+    Xu = buf[1:].view(cu["X"].shape)          # 2 bytes past a 16-byte boundary
+    Xu.copy_(cu["X"])
+    Yu = gs_cuda.gs_deform_conv(Xu, cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) for n in ("X", "W", "offset", "B", "mask")],
+                                 **kw)
+    assert_parity(Y, ref, "bfloat16", "staged")
+    assert_parity(Yu, ref, "bfloat16", "unaligned X, previous kernel")

@@ -35,7 +35,7 @@ cases = []
 for t in range(T):
     th2 = wl.as_dtype(wl.identity_theta(2, 2) + g.normal(0, 0.1, (2, 2, 3)), "bfloat16")
     X2 = wl.as_dtype(g.normal(size=(2, 4, 40, 36)), "bfloat16")
-    th3 = wl.as_dtype(wl.identity_theta(3, 1) + g.normal(0, 0.1, (1, 3, 4)), "float32")
+    th3 = wl.as_dtype(wl.identity_theta(1, 3) + g.normal(0, 0.1, (1, 3, 4)), "float32")
     X3 = wl.as_dtype(g.normal(size=(1, 2, 12, 13, 14)), "float32")
     Xr = wl.as_dtype(g.normal(size=(1, 3, 20, 24)), "bfloat16")
     Xd = wl.as_dtype(g.normal(size=(1, 16, 9, 10)), "bfloat16")
