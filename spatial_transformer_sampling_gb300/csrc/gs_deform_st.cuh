@@ -282,6 +282,7 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
         tma_load_4d(raw_s, &xmap, w.x0, w.y0, cb * kStKC, n, &raw_full);
     };
     // offsets and mask of a tile: planes x 128 positions, 16 bytes per cp.async
+    // (spread over the threads; one committed group per tile)
     auto fetch_taps = [&](int tile) {
         const int n = tile / q.tiles, p0 = (tile - n * q.tiles) * kStM;
         for (int e = tid; e < planes * 16; e += NT) {
@@ -293,21 +294,27 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
             cp_async16(smem_u32(tap_s + pl * kStM + part * 8), src + (valid > 0 ? pbeg : 0),
                        (uint32_t)valid * 2);
         }
+        cp_async_commit();
     };
 
     // start-up: the first chunk's window and the first tile's offsets are in
     // flight while W is repacked
     int tile_id = blockIdx.x;
+    if (tid == 0) tma_prefetch_map(&xmap);
     if (tid == 0) {
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
         mbar_init(&raw_full, 1);
         fence_mbar_init();
-        if (tile_id < q.total) issue_raw(tile_id, 0);
     }
+    __syncthreads();   // no thread waits on a barrier before it is initialised
+    if (tid == 0 && tile_id < q.total) issue_raw(tile_id, 0);
     if (tile_id < q.total) fetch_taps(tile_id);
-    cp_async_commit();
-    if (tid < 32) tmem_alloc(&s_tmem, q.tmem_cols);
+    // the last warp allocates the accumulator, off warp 0's start-up path
+    if (tid >= NT - 32) {
+        tmem_alloc(&s_tmem, q.tmem_cols);
+        tcgen05_fence_before_sync();   // the address is read by others after a barrier
+    }
     // W -> B operand in (k, c) order.  Item (oc, c8): W[oc, 8*c8 .. 8*c8+7, 0..K-1]
     // is 8K contiguous elements (16-byte aligned: C % 16 == 0) and holds, for
     // each kernel tap k, the 16-byte B row of K index k*C + 8*c8 .. +7 for oc,
@@ -433,7 +440,6 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
         __syncthreads();   // every thread has read this tile's offsets
         const int next = tile_id + gridDim.x;
         if (next < q.total) fetch_taps(next);
-        cp_async_commit();
         // owned kernel taps with a window-leaving tap anywhere in the warp
         uint32_t wfb = 0;
 #pragma unroll
@@ -552,7 +558,7 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
     }
     tcgen05_fence_before_sync();
     __syncthreads();
-    if (tid < 32) {
+    if (tid >= NT - 32) {   // the allocating warp releases it
         tcgen05_fence_after_sync();
         tmem_dealloc(s_tmem, q.tmem_cols);
     }

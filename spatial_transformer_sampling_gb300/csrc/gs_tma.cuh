@@ -68,6 +68,12 @@ inline bool tmap_encode(CUtensorMap *map, int elem_bytes, bool bf16, int rank, c
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Starts fetching a tensor map's descriptor (kernel-parameter space) so the
+// first copy that uses it does not wait for it.
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Loads the box at coordinates (c0 innermost .. c3) of a 4-D map into shared
 // memory at dst (128-byte aligned); the bytes complete on `bar`, which the
 // issuing thread armed with mbar_arrive_expect_tx for the box's size.  c0
