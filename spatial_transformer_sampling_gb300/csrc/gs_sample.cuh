@@ -330,6 +330,7 @@ inline Axis make_axis(int n, int ac) {
 #include "gs_nd.cuh"
 #include "gs_nhwc.cuh"
 #include "gs_vol.cuh"
+#include "gs_vol_tma.cuh"
 
 namespace gs {
 
@@ -343,7 +344,9 @@ static cudaError_t launch_sample_t(const void *X, const void *src, void *Y, Samp
     }
     if constexpr (AFFINE && R == 3 && MODE != MODE_CUBIC) {
         bool used = false;
-        const cudaError_t e = launch_vol<T, MODE>(X, src, Y, P, s, &used);
+        cudaError_t e = launch_vol_tma<T, MODE>(X, src, Y, P, s, &used);
+        if (used || e != cudaSuccess) return e;
+        e = launch_vol<T, MODE>(X, src, Y, P, s, &used);
         if (used || e != cudaSuccess) return e;
     }
 
