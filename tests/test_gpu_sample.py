@@ -169,18 +169,24 @@ def test_nearest_half_integer_ties_are_bit_exact(gs_cuda, oracle_mod, dtype, ac,
                                                                    pad, ac))
 
 
-def test_grid_sample_affine_grid_composition(gs_cuda, oracle_mod):
-    """gs_affine_grid feeds gs_grid_sample: the grid is rounded to fp32 in between."""
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("mode", ["linear", "cubic"])
+def test_grid_sample_affine_grid_composition(gs_cuda, oracle_mod, dtype, mode):
+    """gs_affine_grid feeds gs_grid_sample, the unfused composition: the grid is
+    rounded to the I/O dtype in between (the unfused reading), so the sampling stage
+    is compared with the oracle's GridSample on that rounded grid, and the grid with
+    the oracle's AffineGrid."""
     g = wl.rng(81)
     X = g.normal(size=(2, 3, 20, 24))
     theta = wl.identity_theta(2, 2) + g.normal(0, 0.2, size=(2, 2, 3))
     size = (2, 3, 18, 22)
-    Tt = wl.as_dtype(theta, "float32")
+    Tt, Xt = wl.as_dtype(theta, dtype), wl.as_dtype(X, dtype)
     G = gs_cuda.gs_affine_grid(Tt.cuda(), size, 1)
     G_ref = oracle_mod.affine_grid(exact(Tt), size, 1)
-    assert_parity(G, G_ref, "float32", "grid")
-    Y = gs_cuda.gs_grid_sample(dev(X, "float32"), G, "linear", "border", 1)
-    assert Y.shape == (2, 3, 18, 22) and torch.isfinite(Y).all()
+    assert_parity(G, G_ref, dtype, "grid")
+    Y = gs_cuda.gs_grid_sample(Xt.cuda(), G, mode, "border", 1)
+    ref = oracle_mod.grid_sample(exact(Xt), exact(G), mode, "border", 1)
+    assert_parity(Y, ref, dtype, f"sampling the rounded grid ({mode}, {dtype})")
 
 
 # ------------------------------------------------------------- edge cases

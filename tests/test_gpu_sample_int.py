@@ -1,9 +1,8 @@
 """GridSample with integer X (uint8, int8, uint16, int16) on the GPU against the
-oracle.  The oracle interpolates the exact integer values in fp64; the cast at the
-end (truncation toward zero, saturated at the type's range) is compared exactly
-wherever the fp64 value is farther from an integer than the kernel's fp32
-rounding can move it, and within one unit (the two integers around it) elsewhere.
-Nearest-mode outputs are copies and must be bit-exact everywhere."""
+oracle, value for value.  Both sides take the truncating cast at the end from the
+same fp64 value: the library evaluates integer X in fp64 with every product and
+sum rounded on its own, in the oracle's order, so every output -- including those
+next to an integer and those that saturate -- must equal the oracle's cast."""
 import itertools
 import zlib
 
@@ -36,28 +35,11 @@ def _as_int64(t):
         else t.to(torch.int64).numpy()
 
 
-def check_int(oracle_mod, Y, X64, grid64, mode, pad, ac, dtype, r, coverage=True):
+def check_int(oracle_mod, Y, X64, grid64, mode, pad, ac, dtype):
     v = oracle_mod.grid_sample(X64, grid64, mode, pad, ac)
     exp = oracle_mod.cast_to_integer(v, dtype)
-    got = _as_int64(Y.cpu())
-    if mode == "nearest":
-        np.testing.assert_array_equal(got, exp)
-        return
-    # fp32 error bound: one rounding per tap and per axis combine (plus the weight
-    # products), each at most one ulp of |sum w X| <= max|X| * sum|w|
-    taps = (2 if mode == "linear" else 4) ** r
-    wsum = 1.0 if mode == "linear" else 1.6 ** r
-    band = (taps + r) * 2.0 ** -23 * np.abs(X64).max() * wsum + 1e-6
-    lo, hi = oracle_mod.INT_RANGES[dtype]
-    near = np.abs(v - np.round(v)) <= band
-    clear = ~near | (v <= lo - band) | (v >= hi + band)   # clearly saturated
-    np.testing.assert_array_equal(got[clear], exp[clear])
-    lo_exp = oracle_mod.cast_to_integer(v - band, dtype)
-    hi_exp = oracle_mod.cast_to_integer(v + band, dtype)
-    assert ((got >= np.minimum(lo_exp, hi_exp)) & (got <= np.maximum(lo_exp, hi_exp))).all()
-    if coverage and band < 0.05:
-        assert clear.mean() > 0.5   # the exact comparison covers most outputs
-    return band
+    np.testing.assert_array_equal(_as_int64(Y.cpu()), exp)
+    return v
 
 
 SWEEP = [(r, m, p, ac, dt, gdt) for r in (1, 2, 3) for m in ("linear", "nearest", "cubic")
@@ -77,7 +59,7 @@ def test_integer_x_sweep(gs_cuda, oracle_mod, r, mode, pad, ac, dtype, gdt):
     Y = gs_cuda.gs_grid_sample_int(Xt.cuda(), Gt.cuda(), mode, pad, ac)
     assert Y.dtype == Xt.dtype and tuple(Y.shape) == xs[:2] + out
     assert gs_cuda.gs_device_status() == 0
-    check_int(oracle_mod, Y, X64, wl.widened(Gt), mode, pad, ac, dtype, r)
+    check_int(oracle_mod, Y, X64, wl.widened(Gt), mode, pad, ac, dtype)
 
 
 @pytest.mark.parametrize("dtype", list(ITYPES))
@@ -93,12 +75,9 @@ def test_integer_x_cubic_overshoot_saturates(gs_cuda, oracle_mod, dtype):
     Y = gs_cuda.gs_grid_sample_int(Xt.cuda(), Gt.cuda(), "cubic", "border", 0)
     v = oracle_mod.grid_sample(X64, wl.widened(Gt), "cubic", "border", 0)
     assert (v > hi).any() and (v < lo).any()
-    # most outputs sit on the flat sides, exactly on lo or hi: no coverage bar here
-    band = check_int(oracle_mod, Y, X64, wl.widened(Gt), "cubic", "border", 0, dtype, 2,
-                     coverage=False)
+    check_int(oracle_mod, Y, X64, wl.widened(Gt), "cubic", "border", 0, dtype)
     got = _as_int64(Y.cpu())
-    assert (got[v > hi + band] == hi).all() and (got[v < lo - band] == lo).all()
-    assert (v > hi + band).any() and (v < lo - band).any()
+    assert (got[v > hi] == hi).all() and (got[v < lo] == lo).all()
 
 
 def test_integer_x_at_pixel_centres_is_a_copy(gs_cuda, oracle_mod):
@@ -112,3 +91,21 @@ def test_integer_x_at_pixel_centres_is_a_copy(gs_cuda, oracle_mod):
     for mode in ("linear", "cubic"):
         Y = gs_cuda.gs_grid_sample_int(Xt.cuda(), Gt.cuda(), mode, "zeros", 0)
         np.testing.assert_array_equal(_as_int64(Y.cpu()), X64.astype(np.int64))
+
+
+@pytest.mark.parametrize("mode", ["linear", "cubic"])
+def test_integer_x_constant_image_matches_the_fp64_cast(gs_cuda, oracle_mod, mode):
+    """A constant image: the exact interpolated value is the constant itself (linear,
+    and cubic away from the zero border), while its fp64 evaluation can land one ulp
+    below it and truncate to the integer underneath.  The library's value must be the
+    oracle's double, so its cast agrees either way."""
+    X64 = np.full((1, 2, 9, 11), 37.0)
+    Xt = torch.from_numpy(X64.astype(np.int64)).to(torch.uint8)
+    grid = wl.rng(77).uniform(-1.3, 1.3, size=(1, 40, 50, 2))
+    Gt = wl.as_dtype(grid, "float32")
+    for pad in ("zeros", "border"):
+        Y = gs_cuda.gs_grid_sample_int(Xt.cuda(), Gt.cuda(), mode, pad, 0)
+        v = check_int(oracle_mod, Y, X64, wl.widened(Gt), mode, pad, 0, "uint8")
+        if pad == "border" and mode == "linear":
+            # the fp64 sum misses 37 in a share of the outputs: the case this pins
+            assert (v < 37.0).any() and (v == 37.0).any()
