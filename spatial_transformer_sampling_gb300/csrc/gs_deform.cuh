@@ -1,5 +1,7 @@
-// gs_deform.cuh -- DeformConv 2-D with fp32 FMAs (every dtype and attribute;
-// fp16/bf16 shapes the tensor-core kernel in gs_deform_tc.cuh covers go there).
+// gs_deform.cuh -- DeformConv 2-D with fp32 FMAs (every dtype and attribute):
+// the general kernel for the shapes the faster ones do not take (fp16/bf16:
+// the tensor-core kernels of gs_deform_st.cuh and gs_deform_tc.cuh; fp32: the
+// windowed kernel of gs_deform_f32.cu).
 //
 // DeformConv (ai.onnx, since version 22), Inputs: the output is an ordinary
 // convolution over a column of samples, each a bilinear read of X at the
@@ -188,6 +190,11 @@ cudaError_t launch_deform(const void *X, const void *W, const void *offset, cons
         cudaError_t e = launch_deform_staged<T>(X, W, offset, B, mask, Y, a, s, &used);
         if (used || e != cudaSuccess) return e;
         e = launch_deform_tc<T>(X, W, offset, B, mask, Y, a, s, &used);
+        if (used || e != cudaSuccess) return e;
+    } else {
+        // fp32: the windowed register-tiled kernel where the shape allows
+        bool used = false;
+        const cudaError_t e = launch_deform_f32(X, W, offset, B, mask, Y, a, s, &used);
         if (used || e != cudaSuccess) return e;
     }
     const int P = a.oH * a.oW;

@@ -138,6 +138,12 @@ cudaError_t launch_deform_staged(const void *X, const void *W, const void *offse
                                  bool *used);
 bool deform_staged_takes(const DeformArgs &args, const void *X, const void *W, const void *offset,
                          const void *mask);
+// DeformConv (fp32) on the windowed register-tiled kernel (gs_deform_f32.cu)
+// when it takes the shape and X pointer; *used reports whether it ran.
+cudaError_t launch_deform_f32(const void *X, const void *W, const void *offset, const void *B,
+                              const void *mask, void *Y, const DeformArgs &args, cudaStream_t s,
+                              bool *used);
+bool deform_f32_takes(const DeformArgs &args, const void *X);
 template <typename T>
 cudaError_t launch_resize(const void *X, void *Y, const ResizeArgs &args, cudaStream_t s);
 // GridSample with integer X (TX: uint8_t, int8_t, uint16_t, int16_t) and a float

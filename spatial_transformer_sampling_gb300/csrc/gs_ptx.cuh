@@ -104,6 +104,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async through L1); src_bytes 0
+// writes a zero word without reading `src`.  For element-wise transposing
+// copies that 16-byte runs cannot do.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }

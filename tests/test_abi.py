@@ -159,10 +159,15 @@ def test_deform_conv_rejects_bad_arguments(L, kwargs, status, ws):
 def test_deform_conv_workspace_size_queries(L):
     n = ctypes.c_size_t(7)
     a = gs.deform_attrs((3, 3), (1, 1, 1, 1))
-    # bf16, tensor-core shape: packed W (64*64*9*2 bytes) + 8 slots of (64*64 + 1) * 64 * 2
+    # bf16, 3x3: the staged kernel takes the shape and wants no workspace
     assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 2,
+                                           ctypes.byref(n)) == 0 and n.value == 0
+    # bf16, 1x5 (a tap count the staged kernel does not take): the channel-last
+    # path's packed W (64*64*5*2 bytes) + 8 slots of (64*64 + 1) * 64 * 2
+    a5 = gs.deform_attrs((1, 5), (0, 2, 0, 2))
+    assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a5), 2,
                                            ctypes.byref(n)) == 0
-    assert n.value == 64 * 64 * 9 * 2 + 8 * (64 * 64 + 1) * 64 * 2
+    assert n.value == 64 * 64 * 5 * 2 + 8 * (64 * 64 + 1) * 64 * 2
     assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 0,
                                            ctypes.byref(n)) == 0 and n.value == 0   # fp32
     assert L.gs_deform_conv_workspace_size(_i64([8, 64, 64, 64]), 64, ctypes.byref(a), 2,

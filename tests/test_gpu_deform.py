@@ -290,3 +290,89 @@ def test_deform_conv_staged_matches_unaligned_fallback(gs_cuda, oracle_mod):
                                  **kw)
     assert_parity(Y, ref, "bfloat16", "staged")
     assert_parity(Yu, ref, "bfloat16", "unaligned X, previous kernel")
+
+
+# ------------------------------------------------ fp32 windowed kernel
+
+# shapes the fp32 windowed kernel takes (W % 4 == 0, channels per group and
+# per offset group multiples of 8, kH kW <= 9)
+F32_CASES = [
+    # N, C, H, W, oC, kernel, pads, strides, dilations, group, og, bias, mask, offset sigma
+    (2, 16, 24, 32, 64, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True, 1.0),    # 4 rows/tile
+    (1, 24, 10, 128, 40, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True, 1.0),   # 1 row/tile
+    (1, 16, 20, 40, 130, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, False, True, 1.0),  # ragged, 3 oc blocks
+    (2, 32, 16, 16, 32, (1, 1), (0, 0, 0, 0), (1, 1), (1, 1), 1, 1, True, False, 1.0),   # K = 1
+    (1, 16, 33, 48, 16, (2, 2), (1, 0, 0, 1), (2, 2), (2, 1), 1, 1, True, True, 1.0),    # stride, dilation
+    (1, 32, 20, 24, 24, (3, 2), (1, 1, 1, 0), (1, 2), (1, 1), 2, 1, True, True, 1.0),    # 2 groups
+    (2, 32, 16, 16, 32, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 4, True, True, 1.0),    # 4 offset groups
+    (2, 16, 32, 32, 16, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True, 6.0),    # taps leave the window
+    (1, 8, 8, 8, 8, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, False, False, 0.7),      # one partial tile
+    (1, 16, 7, 4, 8, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True, 1.0),       # 4 columns
+    (1, 16, 12, 256, 16, (3, 3), (1, 1, 1, 1), (1, 1), (1, 1), 1, 1, True, True, 1.0),   # wide rows
+    (1, 16, 9, 8, 16, (3, 3), (0, 0, 0, 0), (1, 1), (3, 3), 1, 1, True, True, 1.0),      # dilation 3
+]
+
+
+def _f32_inputs(case, seed):
+    N, C, H, W, oC, k, p, s, d, grp, og, has_b, has_m, sig = F32_CASES[case]
+    g = wl.rng(seed)
+    oH = (H + p[0] + p[2] - d[0] * (k[0] - 1) - 1) // s[0] + 1
+    oW = (W + p[1] + p[3] - d[1] * (k[1] - 1) - 1) // s[1] + 1
+    K = k[0] * k[1]
+    host = {
+        "X": wl.as_dtype(g.normal(size=(N, C, H, W)), "float32"),
+        "W": wl.as_dtype(g.normal(0, 0.05, size=(oC, C // grp) + k), "float32"),
+        "offset": wl.as_dtype(g.normal(0, sig, size=(N, og * K * 2, oH, oW)), "float32"),
+        "B": wl.as_dtype(g.normal(size=(oC,)), "float32") if has_b else None,
+        "mask": wl.as_dtype(1.0 / (1.0 + np.exp(-g.normal(size=(N, og * K, oH, oW)))), "float32")
+        if has_m else None,
+    }
+    return host, dict(kernel_shape=k, pads=p, strides=s, dilations=d, group=grp, offset_group=og)
+
+
+@pytest.mark.parametrize("case", range(len(F32_CASES)))
+def test_deform_conv_f32_window_shapes(gs_cuda, oracle_mod, case):
+    host, kw = _f32_inputs(case, 900 + case)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    args = (cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"])
+    Y = gs_cuda.gs_deform_conv(*args, **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Y, ref, "float32", f"deform fp32 window case {case}")
+    assert torch.equal(Y, gs_cuda.gs_deform_conv(*args, **kw))
+
+
+def test_deform_conv_f32_window_matches_unaligned_fallback(gs_cuda, oracle_mod):
+    """X off the 16-byte alignment the windowed kernel copies with runs the
+    general fp32 kernel; both agree with the oracle and with each other."""
+    host, kw = _f32_inputs(0, 950)
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    buf = torch.empty(cu["X"].numel() + 1, dtype=torch.float32, device="cuda")
+    Xu = buf[1:].view(cu["X"].shape)          # 4 bytes past a 16-byte boundary
+    Xu.copy_(cu["X"])
+    Yu = gs_cuda.gs_deform_conv(Xu, cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) for n in ("X", "W", "offset", "B", "mask")],
+                                 **kw)
+    assert_parity(Y, ref, "float32", "windowed")
+    assert_parity(Yu, ref, "float32", "unaligned X, general kernel")
+    assert_parity(Y, exact(Yu), "float32", "windowed against general")
+
+
+def test_deform_conv_f32_nonfinite_offsets(gs_cuda, oracle_mod):
+    """Offsets that are NaN, infinite or huge give zero samples, as the general
+    kernel and the oracle take them."""
+    host, kw = _f32_inputs(0, 960)
+    off = host["offset"].clone()
+    off.view(-1)[::97] = float("nan")
+    off.view(-1)[5::101] = float("inf")
+    off.view(-1)[9::89] = -3.0e9
+    host["offset"] = off
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    Y = gs_cuda.gs_deform_conv(cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"], **kw)
+    assert gs_cuda.gs_device_status() == 0
+    ref = oracle_mod.deform_conv(*[exact(host[n]) for n in ("X", "W", "offset", "B", "mask")],
+                                 **kw)
+    assert_parity(Y, ref, "float32", "non-finite offsets")
