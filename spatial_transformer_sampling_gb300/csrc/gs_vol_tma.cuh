@@ -31,12 +31,9 @@ constexpr int kVtThreads = 256;
 constexpr int kVtWarps = kVtThreads / 32;
 constexpr int kVtPPT = 4;                          // output positions per thread
 constexpr int kVtTile = kVtThreads * kVtPPT;       // output positions per tile
-constexpr int kVtMaps = 8;                         // tensor maps (box sizes) per launch
-constexpr int kVtMaxStages = 4;
+constexpr int kVtMaps = 9;                         // tensor maps (box sizes) per launch
+constexpr int kVtMaxStages = 8;
 constexpr int kVtRingBytes = 96 * 1024;            // two blocks per SM
-// Box margins along x beyond the nominal extent (elements): the small and the
-// large box of the map family.
-constexpr int kVtMarginX0 = 3, kVtMarginX1 = 11;
 
 struct VolTmaParams {
     int tz, ty, tx;          // tile extents along output depth, rows, columns (tx: 8, 16 or 32)
@@ -341,9 +338,11 @@ cudaError_t launch_vol_tma(const void *X, const void *theta, void *Y, const Samp
     if ((int64_t)a.N * a.C >= ((int64_t)1 << 31)) return cudaSuccess;
     const int Do = a.out[0], Ho = a.out[1], Wo = a.out[2];
     VolTmaParams V;
-    V.tx = Wo > 16 ? 32 : (Wo > 8 ? 16 : 8);
+    // near-cubic tiles: an affine map's box around a tile grows with the
+    // tile's longest side, so 8 x 8 x 16 reads less than 4 x 8 x 32
+    V.tx = Wo >= 16 ? 16 : 8;
     const int rows = kVtTile / V.tx;
-    V.tz = min(Do, V.tx == 32 ? 4 : 8);
+    V.tz = min(Do, 8);
     V.ty = min(Ho, rows / V.tz);
     V.tz = min(Do, rows / V.ty);
     V.tiles_y = (Ho + V.ty - 1) / V.ty;
@@ -352,21 +351,27 @@ cudaError_t launch_vol_tma(const void *X, const void *theta, void *Y, const Samp
     if (tiles * a.N > 0x7fffffffLL) return cudaSuccess;
     V.tiles = (int)tiles;
     V.total = (int)(tiles * a.N);
-    // nominal extents: the tile scaled by in/out, + the neighbour tap (+ x alignment)
+    // nominal extents: the tile scaled by in/out, + the neighbour tap (x in
+    // whole 16-byte runs)
     const int t[3] = {V.tz, V.ty, V.tx};
     const int nin[3] = {Di, Hi, Wi}, nout[3] = {Do, Ho, Wo};
     int nom[3];
-    for (int d = 0; d < 3; ++d)
-        nom[d] = (int)ceil((double)t[d] * nin[d] / nout[d]) + K + (d == 2 ? EPC - 1 : 0);
-    const int margin[3][2] = {{3, 7}, {3, 7}, {kVtMarginX0, kVtMarginX1}};
+    for (int d = 0; d < 3; ++d) {
+        nom[d] = (int)ceil((double)t[d] * nin[d] / nout[d]) + K;
+        if (d == 2) nom[d] = (nom[d] + EPC - 1) / EPC * EPC;
+    }
+    // the family: margins of 1 or 3 on planes and rows, 0 or one 16-byte run
+    // on x, for near-identity maps; and one box with wide margins (7, 7, three
+    // runs) for stronger rotations and zooms.  Wider tiles gather.
     struct Box { int b[3]; int bytes; };
     Box cand[kVtMaps];
     int nc = 0;
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < kVtMaps; ++m) {
         Box bx;
         for (int d = 0; d < 3; ++d) {
-            int v = nom[d] + margin[d][(m >> d) & 1];
-            if (d == 2) v = (v + EPC - 1) / EPC * EPC;
+            const int bit = (m >> d) & 1;
+            int v = m == 8 ? nom[d] + (d == 2 ? 3 * EPC : 7)
+                           : nom[d] + (d == 2 ? bit * EPC : (bit ? 3 : 1));
             bx.b[d] = min(v, 256);
         }
         bx.bytes = (bx.b[0] * bx.b[1] * bx.b[2] * E + 127) & ~127;
