@@ -86,13 +86,19 @@ def peaks():
                 "source": "fallback"}
 
 
+# CUDA sources each kernel is built from (most specific tag prefix first).
 KERNEL_SOURCES = {
     "band_kernel": ["gs_band.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
-    "sample_kernel": ["gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "nhwc_sample_kernel": ["gs_nhwc.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_internal.h"],
-    "deform": ["gs_deform.cuh", "gs_deform_tc.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "sample_kernel": ["gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "deform_tc_nhwc": ["gs_deform_tc.cuh", "gs_copy.cuh", "gs_common.cuh", "gs_ptx.cuh",
                        "gs_internal.h"],
+    "deform_st_kernel": ["gs_deform_st.cuh", "gs_tma.cuh", "gs_common.cuh", "gs_ptx.cuh",
+                         "gs_internal.h"],
+    "deform_f32_kernel": ["gs_deform_f32.cu", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "deform": ["gs_deform.cuh", "gs_deform_tc.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
+    "vol_tma_kernel": ["gs_vol_tma.cuh", "gs_vol.cuh", "gs_tma.cuh", "gs_sample.cuh",
+                       "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "vol_kernel": ["gs_vol.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "resize_kernel": ["gs_resize.cuh", "gs_common.cuh", "gs_internal.h"],
 }
@@ -245,7 +251,8 @@ class Case:
             if w.r == 2:
                 self.kernel_tag = f"band_kernel<{DT_SHORT[dtype]},{self.mode}>"
             elif self.mode != "cubic":
-                self.kernel_tag = f"vol_kernel<{DT_SHORT[dtype]},{self.mode}>"
+                # the TMA-staged kernel (inputs 16-byte aligned, rows in whole 16-byte runs)
+                self.kernel_tag = f"vol_tma_kernel<{DT_SHORT[dtype]},{self.mode}>"
             else:
                 self.kernel_tag = f"sample_kernel<{DT_SHORT[dtype]},{w.r},{self.mode},affine>"
         elif w.kind == "grid_sample":
@@ -271,7 +278,10 @@ class Case:
             oW = (W_ + w.pads[1] + w.pads[3] - (w.kernel[1] - 1) - 1) // w.strides[1] + 1
             self.outputs = N * w.oc * oH * oW
             self.flops = 2.0 * N * oH * oW * w.oc * (C // w.group) * w.kernel[0] * w.kernel[1]
-            self.kernel_tag = f"deform<{DT_SHORT[dtype]}>"
+            # the kernels the plain call takes for this shape (3x3, C and oC multiples
+            # of 16, group 1): windowed FFMA for fp32, staged tcgen05 for 16-bit types
+            self.kernel_tag = (f"deform_f32_kernel<{DT_SHORT[dtype]}>" if dtype == "float32"
+                               else f"deform_st_kernel<{DT_SHORT[dtype]}>")
             if workspace:
                 a = gs.deform_attrs(w.kernel, w.pads, w.strides, w.dilations, w.group,
                                     w.offset_group)
@@ -402,8 +412,20 @@ def time_e2e(case, steps, warmup):
     return ms, h2d, d2h
 
 
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
+# (the GB300's SM count and maximum SM clock); the bound of the fp32 DeformConv
+# kernel, whose contraction runs on FFMA.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def roofline_for(case, ms, pk):
-    if case.w.kind == "deform_conv" and case.dtype != "float32":
+    if case.w.kind == "deform_conv" and case.dtype == "float32":
+        achieved = case.flops / (ms * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": round(achieved, 3), "peak": round(FP32_ALU_TFLOPS, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 4),
+                "traffic": recorded_traffic(case.kernel_tag, case.name, case.dtype),
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x 2.07 GHz"}
+    if case.w.kind == "deform_conv":
         achieved = case.flops / (ms * 1e-3) / 1e12
         peak = pk["bf16_tflops"]
         return {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,

@@ -34,8 +34,13 @@ def test_deform_conv_in_16_bit_is_tensor_bound(monkeypatch):
     assert r["achieved"] == pytest.approx(200.0)    # 2 TFLOP in 10 ms
     assert r["frac"] == pytest.approx(0.1)
     assert r["traffic"] == 123.0
-    # fp32 DeformConv has no tensor-core path: it is reported against HBM
-    assert bench.roofline_for(_case(kind="deform_conv"), 1.0, PEAKS)["bound"] == "hbm"
+    # fp32 DeformConv contracts on FFMA: reported against the fp32 FMA peak
+    # derived from the SM count and clock (152 x 128 x 2 x 2.07 GHz)
+    r32 = bench.roofline_for(_case(kind="deform_conv", dtype="float32", flops=8.0e9), 1.0, PEAKS)
+    assert r32["bound"] == "alu" and r32["unit"] == "TFLOP/s"
+    assert r32["achieved"] == pytest.approx(8.0)    # 8 GFLOP in 1 ms
+    assert r32["peak"] == pytest.approx(80.5, abs=0.1)
+    assert r32["frac"] == pytest.approx(8.0 / (152 * 128 * 2 * 2.07e9 / 1e12), rel=1e-3)
 
 
 def _tree(tmp_path, source="int a;"):
