@@ -406,10 +406,16 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
         uint32_t off[TG][2];   // byte offsets of taps 2h, 2h+1: low, high half
         float wt[TG][4];
         uint32_t fb = 0;       // bit 4i+t: tap t of owned kernel tap i leaves the window
-        int kh = k0 / a.kW, kw = k0 - (k0 / a.kW) * a.kW;
+        // The two threads of a position (channel octets j = 0, 1; adjacent
+        // lanes) need the same taps: each computes every other owned kernel
+        // tap, for the slot's first half, and they swap results; the second
+        // octet's offsets are the first's with the half bit flipped.
+        constexpr int TP = (TG + 1) / 2;   // owned kernel taps computed per thread
 #pragma unroll
-        for (int i = 0; i < TG; ++i) {
-            const int k = min(k0 + i, K - 1);   // a tap past the group's end is never used
+        for (int s2 = 0; s2 < TP; ++s2) {
+            const int i_mine = 2 * s2 + j;
+            const int k = min(k0 + i_mine, K - 1);   // a tap past the group's end is never used
+            const int kh = k / a.kW, kw = k - kh * a.kW;
             const float dy = IO<T>::to_float(tap_s[(2 * k) * kStM + pl]);
             const float dx = IO<T>::to_float(tap_s[(2 * k + 1) * kStM + pl]);
             const float m = a.has_mask ? IO<T>::to_float(tap_s[(2 * K + k) * kStM + pl]) : 1.0f;
@@ -417,25 +423,50 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
             float w[4];
             bool in[4];
             st_taps(a, oh, ow, kh, kw, dy, dx, m, yy, xx, w, in);
-            if (++kw == a.kW) {
-                kw = 0;
-                ++kh;
-            }
             uint32_t o[4];
+            float wm[4];
+            uint32_t bits = 0;
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const bool ok = live && in[t];
-                wt[i][t] = ok ? w[t] : 0.0f;
+                wm[t] = ok ? w[t] : 0.0f;
                 const uint32_t ry = (uint32_t)(yy[t] - win.y0), rx = (uint32_t)(xx[t] - win.x0);
                 if (ok && ry < (uint32_t)rows && rx < (uint32_t)cols) {
-                    o[t] = st_half(ry * (uint32_t)cols + rx, (uint32_t)j);
+                    o[t] = st_half(ry * (uint32_t)cols + rx, 0u);
                 } else {
                     o[t] = kStZeroOff;   // outside the image, or read again below
-                    if (ok) fb |= 1u << (4 * i + t);
+                    if (ok) bits |= 1u << t;
                 }
             }
-            off[i][0] = o[0] | (o[1] << 16);
-            off[i][1] = o[2] | (o[3] << 16);
+            const uint32_t m0 = o[0] | (o[1] << 16), m1 = o[2] | (o[3] << 16);
+            // the partner's tap (index 2 s2 + 1 - j)
+            const uint32_t p0 = __shfl_xor_sync(0xFFFFFFFFu, m0, 1);
+            const uint32_t p1 = __shfl_xor_sync(0xFFFFFFFFu, m1, 1);
+            const uint32_t pb = __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+            float pw[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) pw[t] = __shfl_xor_sync(0xFFFFFFFFu, wm[t], 1);
+            const int ia = 2 * s2, ib = 2 * s2 + 1;   // even and odd owned tap
+            off[ia][0] = j ? p0 : m0;
+            off[ia][1] = j ? p1 : m1;
+            fb |= (j ? pb : bits) << (4 * ia);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) wt[ia][t] = j ? pw[t] : wm[t];
+            if (ib < TG) {
+                off[ib][0] = j ? m0 : p0;
+                off[ib][1] = j ? m1 : p1;
+                fb |= (j ? bits : pb) << (4 * ib);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) wt[ib][t] = j ? wm[t] : pw[t];
+            }
+        }
+        // this thread's octet: the slot's second half for j = 1 (the zero
+        // pixel's two halves are both zero)
+        const uint32_t hmask = j ? 0x00100010u : 0u;
+#pragma unroll
+        for (int i = 0; i < TG; ++i) {
+            off[i][0] ^= hmask;
+            off[i][1] ^= hmask;
         }
         __syncthreads();   // every thread has read this tile's offsets
         const int next = tile_id + gridDim.x;
