@@ -113,16 +113,19 @@ struct StTranspose {
     uint32_t dst[ITEMS];   // pixel index q0 of the item's first column | channel pair << 24
     uint32_t plane;        // bytes of one channel plane of the raw stage
 
-    __device__ __forceinline__ void setup(int rows, int rw, int tid) {
+    // Thread t of the nthreads transposing threads (t < 0: none) takes items
+    // t, t + nthreads, ...
+    __device__ __forceinline__ void setup(int rows, int rw, int t, int nthreads) {
         const int gpr = rw >> 3;   // 8-column groups per row
-        const int items = rows * gpr * 8;
+        const int items = t < 0 ? 0 : rows * gpr * 8;
         plane = (uint32_t)(rows * rw * 2);
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i) {
-            const int it = tid + i * NT;
+            const int it = t + i * nthreads;
             const int g = it % gpr, rest = it / gpr;
             const int cp = rest & 7, r = rest >> 3;
-            src[i] = it < items ? (uint32_t)(2 * cp) * plane + (uint32_t)(r * rw + 8 * g) * 2 : ~0u;
+            src[i] = t >= 0 && it < items ? (uint32_t)(2 * cp) * plane + (uint32_t)(r * rw + 8 * g) * 2
+                                           : ~0u;
             dst[i] = (uint32_t)(r * rw + 8 * g) | ((uint32_t)cp << 24);
         }
     }
@@ -247,7 +250,9 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
     constexpr int G = st_groups(K);
     constexpr int TG = (K + G - 1) / G;             // kernel taps per thread (at most)
     constexpr int NT = 256 * G;                     // threads
-    constexpr int ITEMS = (kStWinPx + NT - 1) / NT; // window transpose items per thread
+    // the window transpose runs on warps 1.., so that thread 0's MMA issue for
+    // the previous chunk overlaps the other warps' share
+    constexpr int ITEMS = (kStWinPx + NT - 33) / (NT - 32); // window transpose items per thread
     extern __shared__ __align__(128) unsigned char st_smem[];
     __shared__ __align__(8) uint64_t mma_done[2];
     __shared__ __align__(8) uint64_t raw_full;
@@ -357,7 +362,7 @@ deform_st_kernel(const T *__restrict__ X, const T *__restrict__ Wt, const T *__r
     const int ntap = min(TG, K - k0);                // and how many it owns (warp-uniform)
     const uint32_t idesc = umma_idesc_f16(std::is_same<T, __nv_bfloat16>::value, kStM, oC);
     StTranspose<NT, ITEMS> tr;
-    tr.setup(rows, cols, tid);
+    tr.setup(rows, cols, tid - 32, NT - 32);
 
     uint32_t g = 0;          // chunks done by this CTA (A buffer = g % 2, raw phase = g % 2)
     bool aborted = false;    // a bounded wait gave up (agreed on at a barrier)
