@@ -100,7 +100,7 @@ KERNEL_SOURCES = {
     "vol_tma_kernel": ["gs_vol_tma.cuh", "gs_vol.cuh", "gs_tma.cuh", "gs_sample.cuh",
                        "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
     "vol_kernel": ["gs_vol.cuh", "gs_sample.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
-    "resize_kernel": ["gs_resize.cuh", "gs_common.cuh", "gs_internal.h"],
+    "resize_": ["gs_resize.cuh", "gs_common.cuh", "gs_ptx.cuh", "gs_internal.h"],
 }
 
 
@@ -271,7 +271,16 @@ class Case:
             self.outputs = w.x_shape[0] * w.x_shape[1] * int(np.prod(w.out_spatial))
             self.resize_kw = dict(scales=list(w.extra["scales"]), mode=self.mode,
                                   antialias=w.extra["antialias"])
-            self.kernel_tag = f"resize_kernel<{DT_SHORT[dtype]},{w.r},{self.mode}>"
+            # the kernel gs_resize takes for these shapes: 16-bit types with an even
+            # output width up to 512 pair outputs; fp32 with at most four taps per
+            # output stays on the row kernel; the rest (antialias) is staged
+            if eb == 2 and w.out_spatial[-1] % 2 == 0 and w.out_spatial[-1] <= 512:
+                kname = "resize_pair_kernel"
+            elif eb == 4 and not w.extra["antialias"]:
+                kname = "resize_rows_kernel"
+            else:
+                kname = "resize_stage_kernel"
+            self.kernel_tag = f"{kname}<{DT_SHORT[dtype]},{w.r},{self.mode}>"
         else:
             N, C, H, W_ = w.x_shape
             oH = (H + w.pads[0] + w.pads[2] - (w.kernel[0] - 1) - 1) // w.strides[0] + 1
