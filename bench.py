@@ -450,12 +450,13 @@ def roofline_for(case, ms, pk):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(case, budget_s=12.0):
+def oracle_sample(case, budget_s=12.0, threads=None):
     """Time the oracle on a bounded slice of the workload: whole images, doubling the
-    count (and cycling through the batch) until about budget_s of CPU time is spent."""
+    count (and cycling through the batch) until about budget_s of CPU time is spent.
+    threads: OpenMP threads (default every host core, whatever OMP_NUM_THREADS says)."""
     import oracle
     w = case.w
-    threads = oracle.num_procs()   # every host core, whatever OMP_NUM_THREADS says
+    threads = threads or oracle.num_procs()
     oracle.set_num_threads(threads)
     if not hasattr(case, "host64"):   # widen once; each step reuses it
         case.host64 = {k: wl.widened(v) for k, v in case.host.items()}
@@ -589,6 +590,11 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = oracle_sample(case) if rank == 0 and world == 1 else None   # N=1 only
+    if cpu is not None:
+        # the same oracle on one core (a shorter sample), beside the all-core figure
+        one = oracle_sample(case, budget_s=min(args.sample_seconds, 12.0) / 4, threads=1)
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                "sample": one["sample"]}
     if world > 1:
         dist.barrier()
     if rank == 0:
