@@ -376,3 +376,20 @@ def test_deform_conv_f32_nonfinite_offsets(gs_cuda, oracle_mod):
     ref = oracle_mod.deform_conv(*[exact(host[n]) for n in ("X", "W", "offset", "B", "mask")],
                                  **kw)
     assert_parity(Y, ref, "float32", "non-finite offsets")
+
+
+def test_deform_conv_f32_window_unaligned_output(gs_cuda, oracle_mod):
+    """Y four bytes off a 16-byte boundary takes the windowed kernel's scalar
+    stores: the same bits as the vector stores, and the oracle's values."""
+    host, kw = _f32_inputs(2, 970)   # 20 x 40 output, 130 output channels
+    cu = {n: (t.cuda() if t is not None else None) for n, t in host.items()}
+    args = (cu["X"], cu["W"], cu["offset"], cu["B"], cu["mask"])
+    Y = gs_cuda.gs_deform_conv(*args, **kw)
+    buf = torch.empty(Y.numel() + 1, dtype=torch.float32, device="cuda")
+    Yu = buf[1:].view(Y.shape)
+    gs_cuda.gs_deform_conv(*args, out=Yu, **kw)
+    assert gs_cuda.gs_device_status() == 0
+    assert torch.equal(Y, Yu)
+    ref = oracle_mod.deform_conv(*[exact(host[n]) if host[n] is not None else None
+                                   for n in ("X", "W", "offset", "B", "mask")], **kw)
+    assert_parity(Yu, ref, "float32", "unaligned Y")

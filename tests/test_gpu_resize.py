@@ -205,3 +205,20 @@ def test_full_size_resize_workloads(gs_cuda, oracle_mod, name, dtype):
     for n, c in ((0, 0), (w.x_shape[0] - 1, w.x_shape[1] - 1)):
         ref = oracle_mod.resize(wl.widened(Xt[n:n + 1, c:c + 1]), **kw)
         assert_parity(Y[n:n + 1, c:c + 1], ref, dtype, f"{name} slice {n},{c}")
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+def test_resize_pairs_match_single_outputs(gs_cuda, oracle_mod, dtype):
+    """16-bit Resize with an even output width writes pairs of outputs; Y two
+    bytes off a pair boundary takes the single-output staged loop instead.  The
+    same bits either way (each pair lane rounds as fmaf), and the oracle's."""
+    g = wl.rng(zlib.crc32(repr(("pairs", dtype)).encode()))
+    Xt = wl.as_dtype(g.normal(size=(2, 7, 24, 32)), dtype)
+    kw = dict(scales=_f32([1, 1, 2.0, 1.5]), mode="linear")
+    Y1 = gs_cuda.gs_resize(Xt.cuda(), **kw)
+    buf = torch.empty(Y1.numel() + 1, dtype=Y1.dtype, device="cuda")
+    Y2 = buf[1:].view(Y1.shape)
+    gs_cuda.gs_resize(Xt.cuda(), out=Y2, **kw)
+    assert gs_cuda.gs_device_status() == 0
+    assert torch.equal(Y1, Y2)
+    assert_parity(Y1, oracle_mod.resize(wl.widened(Xt), **kw), dtype, f"pairs {dtype}")
