@@ -563,6 +563,55 @@ constexpr int kRsStageRing = 48 * 1024;   // four blocks per SM
 constexpr int kRsStageMax = 16;
 constexpr int kRsStageRows = 32;          // output rows per band, at most
 
+// Thread 0 of a staged block: the input rows the band's taps read (rows set
+// to extrapolation_value read none), the stages of that many rows that fit
+// the ring, the stage barriers, and the copies of the first slices, one bulk
+// async copy per slice.
+template <typename T, int KY>
+__device__ __forceinline__ void rs_ring_start(const T *__restrict__ X, const int *yi,
+                                              const unsigned char *yf, int y0, int y1, int64_t b0,
+                                              int nb, int64_t in_slice, int W, uint32_t row_bytes,
+                                              unsigned char *ring, uint64_t *full, int *r0,
+                                              int *rows, int *stages_out) {
+    int lo = 0x7fffffff, hi = -1;
+    for (int y = y0; y < y1; ++y) {
+        if (yf[y]) continue;
+        for (int k = 0; k < KY; ++k) {
+            lo = min(lo, yi[y * KY + k]);
+            hi = max(hi, yi[y * KY + k]);
+        }
+    }
+    if (hi < 0) lo = hi = 0;
+    const uint32_t stage = (uint32_t)(hi - lo + 1) * row_bytes;
+    const int stages = min(kRsStageMax, (int)(kRsStageRing / stage));   // >= 2 (host)
+    for (int st = 0; st < kRsStageMax; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+    const T *src = X + b0 * in_slice + (int64_t)lo * W;
+    for (int st = 0; st < stages && st < nb; ++st) {
+        mbar_arrive_expect_tx(&full[st], stage);
+        bulk_copy_g2s(ring + (size_t)st * stage, src + (int64_t)st * in_slice, stage, &full[st]);
+    }
+    *r0 = lo;
+    *rows = hi - lo + 1;
+    *stages_out = stages;
+}
+
+// All threads of a staged block: the band's row taps in shared memory (byte
+// offsets within a stage, weights, extrapolation flags), read once per block
+// rather than from the parameter table for every slice.
+template <int KY>
+__device__ __forceinline__ void rs_band_rows(const int *yi, const float *yw, const unsigned char *yf,
+                                             int y0, int y1, int r0, uint32_t row_bytes,
+                                             uint32_t *s_ry, float *s_wy, int *s_fy) {
+    for (int e = threadIdx.x; e < (y1 - y0) * KY; e += kRsThreads) {
+        const int y = y0 + e / KY, k = e - (e / KY) * KY;
+        // rows set to extrapolation_value never read their (zero) offsets
+        s_ry[e] = yf[y] ? 0u : (uint32_t)(yi[y * KY + k] - r0) * row_bytes;
+        s_wy[e] = yw[y * KY + k];
+        if (k == 0) s_fy[e / KY] = yf[y];
+    }
+}
+
 template <typename T, int KY, int KX, int G>
 __global__ void __launch_bounds__(kRsThreads, 4)
 resize_stage_kernel(const T *__restrict__ X, T *__restrict__ Y,
@@ -594,28 +643,8 @@ resize_stage_kernel(const T *__restrict__ X, T *__restrict__ Y,
     const uint32_t row_bytes = (uint32_t)W * (uint32_t)sizeof(T);
 
     if (tid == 0) {
-        // input rows of the band's taps (rows set to extrapolation_value read none)
-        int lo = 0x7fffffff, hi = -1;
-        for (int y = y0; y < y1; ++y) {
-            if (yf[y]) continue;
-            for (int k = 0; k < KY; ++k) {
-                lo = min(lo, yi[y * KY + k]);
-                hi = max(hi, yi[y * KY + k]);
-            }
-        }
-        if (hi < 0) lo = hi = 0;
-        const uint32_t stage = (uint32_t)(hi - lo + 1) * row_bytes;
-        const int stages = min(kRsStageMax, (int)(kRsStageRing / stage));   // >= 2 (host)
-        for (int st = 0; st < kRsStageMax; ++st) mbar_init(&full[st], 1);
-        fence_mbar_init();
-        const T *src = X + b0 * in_slice + (int64_t)lo * W;
-        for (int st = 0; st < stages && st < nb; ++st) {
-            mbar_arrive_expect_tx(&full[st], stage);
-            bulk_copy_g2s(rs_smem + (size_t)st * stage, src + (int64_t)st * in_slice, stage, &full[st]);
-        }
-        s_r0 = lo;
-        s_rows = hi - lo + 1;
-        s_stages = stages;
+        rs_ring_start<T, KY>(X, yi, yf, y0, y1, b0, nb, in_slice, W, row_bytes, rs_smem, full,
+                             &s_r0, &s_rows, &s_stages);
         s_abort = 0;
     }
 
@@ -639,13 +668,7 @@ resize_stage_kernel(const T *__restrict__ X, T *__restrict__ Y,
     __syncthreads();
     const int S = s_stages, r0 = s_r0;
     const uint32_t stage_bytes = (uint32_t)s_rows * row_bytes;
-    for (int e = tid; e < (y1 - y0) * KY; e += kRsThreads) {
-        const int y = y0 + e / KY, k = e - (e / KY) * KY;
-        // rows set to extrapolation_value never read their (zero) offsets
-        s_ry[e] = yf[y] ? 0u : (uint32_t)(yi[y * KY + k] - r0) * row_bytes;
-        s_wy[e] = yw[y * KY + k];
-        if (k == 0) s_fy[e / KY] = yf[y];
-    }
+    rs_band_rows<KY>(yi, yw, yf, y0, y1, r0, row_bytes, s_ry, s_wy, s_fy);
     __syncthreads();
     const uint32_t ring = smem_u32(rs_smem);
     const T *src = X + b0 * in_slice + (int64_t)r0 * W;
@@ -781,30 +804,9 @@ resize_pair_kernel(const T *__restrict__ X, T *__restrict__ Y,
     const int64_t in_slice = (int64_t)H * W, out_slice = (int64_t)ny * nx;
     const uint32_t row_bytes = (uint32_t)W * (uint32_t)sizeof(T);
 
-    if (tid == 0) {
-        // input rows of the band's taps (rows set to extrapolation_value read none)
-        int lo = 0x7fffffff, hi = -1;
-        for (int y = y0; y < y1; ++y) {
-            if (yf[y]) continue;
-            for (int k = 0; k < KY; ++k) {
-                lo = min(lo, yi[y * KY + k]);
-                hi = max(hi, yi[y * KY + k]);
-            }
-        }
-        if (hi < 0) lo = hi = 0;
-        const uint32_t stage = (uint32_t)(hi - lo + 1) * row_bytes;
-        const int stages = min(kRsStageMax, (int)(kRsStageRing / stage));   // >= 2 (host)
-        for (int st = 0; st < kRsStageMax; ++st) mbar_init(&full[st], 1);
-        fence_mbar_init();
-        const T *src = X + b0 * in_slice + (int64_t)lo * W;
-        for (int st = 0; st < stages && st < nb; ++st) {
-            mbar_arrive_expect_tx(&full[st], stage);
-            bulk_copy_g2s(rs_smem + (size_t)st * stage, src + (int64_t)st * in_slice, stage, &full[st]);
-        }
-        s_r0 = lo;
-        s_rows = hi - lo + 1;
-        s_stages = stages;
-    }
+    if (tid == 0)
+        rs_ring_start<T, KY>(X, yi, yf, y0, y1, b0, nb, in_slice, W, row_bytes, rs_smem, full,
+                             &s_r0, &s_rows, &s_stages);
 
     // this thread's column pair and first row of each pass
     const int npairs = nx >> 1;
@@ -836,13 +838,7 @@ resize_pair_kernel(const T *__restrict__ X, T *__restrict__ Y,
     __syncthreads();
     const int S = s_stages, r0 = s_r0;
     const uint32_t stage_bytes = (uint32_t)s_rows * row_bytes;
-    for (int e = tid; e < (y1 - y0) * KY; e += kRsThreads) {
-        const int y = y0 + e / KY, k = e - (e / KY) * KY;
-        // rows set to extrapolation_value never read their (zero) offsets
-        s_ry[e] = yf[y] ? 0u : (uint32_t)(yi[y * KY + k] - r0) * row_bytes;
-        s_wy[e] = yw[y * KY + k];
-        if (k == 0) s_fy[e / KY] = yf[y];
-    }
+    rs_band_rows<KY>(yi, yw, yf, y0, y1, r0, row_bytes, s_ry, s_wy, s_fy);
     __syncthreads();
     const uint32_t ring = smem_u32(rs_smem);
     const T *src = X + b0 * in_slice + (int64_t)r0 * W;
