@@ -4,8 +4,9 @@ The library's only host-side state is per-device setup done by the first call
 that needs it (kernel shared-memory limits, the error word's and the static
 scratch's device addresses), kept in atomics.  A fresh process starts eight
 threads that all make their first calls together, each on its own CUDA stream,
-through the fused 2-D and 3-D paths, the staged Resize kernel and the
-channel-last DeformConv; every result is then compared with the oracle."""
+through the fused 2-D path, both 3-D kernels (gather and TMA-staged boxes),
+the staged Resize kernel, and the staged, channel-last and fp32 windowed
+DeformConv kernels; every result is then compared with the oracle."""
 import os
 import subprocess
 import sys
@@ -41,12 +42,20 @@ for t in range(T):
     Xd = wl.as_dtype(g.normal(size=(1, 16, 9, 10)), "bfloat16")
     Wd = wl.as_dtype(g.normal(0, 0.05, size=(16, 16, 3, 3)), "bfloat16")
     Od = wl.as_dtype(g.normal(0, 1, size=(1, 18, 9, 10)), "bfloat16")
-    cases.append((th2, X2, th3, X3, Xr, Xd, Wd, Od))
+    # widths in whole 16-byte runs: the TMA 3-D kernel, the staged bf16 and the
+    # windowed fp32 DeformConv
+    X3b = wl.as_dtype(g.normal(size=(1, 2, 12, 13, 16)), "float32")
+    Xs = wl.as_dtype(g.normal(size=(1, 16, 9, 16)), "bfloat16")
+    Os = wl.as_dtype(g.normal(0, 1, size=(1, 18, 9, 16)), "bfloat16")
+    Xf = wl.as_dtype(g.normal(size=(1, 16, 9, 16)), "float32")
+    Wf = wl.as_dtype(g.normal(0, 0.05, size=(16, 16, 3, 3)), "float32")
+    Of = wl.as_dtype(g.normal(0, 1, size=(1, 18, 9, 16)), "float32")
+    cases.append((th2, X2, th3, X3, Xr, Xd, Wd, Od, X3b, Xs, Os, Xf, Wf, Of))
 results = [None] * T
 start = threading.Barrier(T)
 
 def work(t):
-    th2, X2, th3, X3, Xr, Xd, Wd, Od = [c.to(dev) for c in cases[t]]
+    th2, X2, th3, X3, Xr, Xd, Wd, Od, X3b, Xs, Os, Xf, Wf, Of = [c.to(dev) for c in cases[t]]
     s = torch.cuda.Stream(dev)
     torch.cuda.synchronize(dev)
     start.wait()
@@ -54,7 +63,10 @@ def work(t):
         r = (gs.gs_affine_sample(th2, (2, 4, 30, 34), X2, "linear", "border", 1),
              gs.gs_affine_sample(th3, (1, 2, 10, 11, 12), X3, "linear", "zeros", 0),
              gs.gs_resize(Xr, scales=(1, 1, 2, 2), mode="linear"),
-             gs.gs_deform_conv(Xd, Wd, Od, pads=(1, 1, 1, 1), workspace="auto"))
+             gs.gs_deform_conv(Xd, Wd, Od, pads=(1, 1, 1, 1), workspace="auto"),
+             gs.gs_affine_sample(th3, (1, 2, 10, 11, 12), X3b, "linear", "zeros", 0),
+             gs.gs_deform_conv(Xs, Wd, Os, pads=(1, 1, 1, 1)),
+             gs.gs_deform_conv(Xf, Wf, Of, pads=(1, 1, 1, 1)))
     s.synchronize()
     results[t] = [y.cpu() for y in r]
 
@@ -63,8 +75,8 @@ for th in threads: th.start()
 for th in threads: th.join()
 assert gs.gs_device_status() == 0
 for t in range(T):
-    th2, X2, th3, X3, Xr, Xd, Wd, Od = [wl.widened(c) for c in cases[t]]
-    y2, y3, yr, yd = results[t]
+    th2, X2, th3, X3, Xr, Xd, Wd, Od, X3b, Xs, Os, Xf, Wf, Of = [wl.widened(c) for c in cases[t]]
+    y2, y3, yr, yd, y3b, ys, yf = results[t]
     assert_parity(y2, oracle.affine_sample(th2, (2, 4, 30, 34), X2, "linear", "border", 1),
                   "bfloat16", f"thread {t} affine 2-D")
     assert_parity(y3, oracle.affine_sample(th3, (1, 2, 10, 11, 12), X3, "linear", "zeros", 0),
@@ -73,6 +85,12 @@ for t in range(T):
                   "bfloat16", f"thread {t} resize")
     assert_parity(yd, oracle.deform_conv(Xd, Wd, Od, pads=(1, 1, 1, 1)), "bfloat16",
                   f"thread {t} deform")
+    assert_parity(y3b, oracle.affine_sample(th3, (1, 2, 10, 11, 12), X3b, "linear", "zeros", 0),
+                  "float32", f"thread {t} affine 3-D, staged boxes")
+    assert_parity(ys, oracle.deform_conv(Xs, Wd, Os, pads=(1, 1, 1, 1)), "bfloat16",
+                  f"thread {t} deform, staged")
+    assert_parity(yf, oracle.deform_conv(Xf, Wf, Of, pads=(1, 1, 1, 1)), "float32",
+                  f"thread {t} deform fp32, windowed")
 print("threads ok")
 """
 
