@@ -925,14 +925,18 @@ resize_pair_kernel(const T *__restrict__ X, T *__restrict__ Y,
     }
 }
 
+// 16-bit types with an even output width up to 512 and Y aligned to a pair
+// run resize_pair_kernel (two outputs per thread on packed FMAs).
+template <typename T> inline bool rs_takes_pair(int nx, const void *Y) {
+    return sizeof(T) == 2 && nx % 2 == 0 && nx <= 2 * kRsThreads &&
+           (uintptr_t)Y % (2 * sizeof(T)) == 0;
+}
+
 template <typename T, int KY, int KX, int G>
 static cudaError_t launch_stage_g(const T *X, T *Y, const ResizeTables &tb, const ResizeArgs &p,
                                   dim3 grid, int rows, int per, unsigned *err, cudaStream_t s) {
     const int H = p.r == 2 ? p.ax[1].n_in : 1, W = p.ax[2].n_in;
-    // 16-bit types with an even output width up to 512 and Y aligned to a
-    // pair: two outputs per thread on packed FMAs
-    if (sizeof(T) == 2 && tb.nx % 2 == 0 && tb.nx <= 2 * kRsThreads &&
-        (uintptr_t)Y % (2 * sizeof(T)) == 0) {
+    if (rs_takes_pair<T>(tb.nx, Y)) {
         static DeviceFlags pair_set;
         const cudaError_t e = once_per_device(pair_set, [] {
             return cudaFuncSetAttribute(resize_pair_kernel<T, KY, KX, G>,
@@ -1006,12 +1010,26 @@ cudaError_t launch_resize_stage(const void *X, void *Y, const ResizeArgs &p, uns
     const size_t stage = (size_t)max_rows(rows) * W * sizeof(T);
     if (2 * stage > (size_t)kRsStageRing) return cudaSuccess;
     const int stages = (int)std::min<size_t>(kRsStageMax, kRsStageRing / stage);
-    // slices per block: about six blocks per SM slot-wave; fewer, longer
-    // blocks keep each block's copies in flight behind its own work (2x
-    // bilinear bf16: 4 slices per block 93.9 us, 8: 83.8 us, 16: 93.2 us)
+    // Slices per block.  The pair kernel: about six blocks per SM slot-wave;
+    // fewer, longer blocks keep each block's copies in flight behind its own
+    // work (2x bilinear bf16: 4 slices per block 93.9 us, 8: 83.8 us, 16:
+    // 93.2 us; one wave of resident blocks, 14: 85.4 us).  resize_stage_kernel:
+    // one wave of resident blocks (four per SM), so each block fills and
+    // drains its ring once (antialiased 1/2 fp32: 16 slices per block over
+    // 1.7 waves 97.6 us, one wave of 27 slices per block 89.5 us).
+    const int64_t nbands = (ny + rows - 1) / rows;
     int64_t per = 64;
-    auto blocks = [&](int64_t p_) { return (int64_t)((ny + rows - 1) / rows) * ((p.B + p_ - 1) / p_); };
-    while (per > 1 && blocks(per) < 6 * 152) per >>= 1;
+    if (rs_takes_pair<T>(tb.nx, Y)) {
+        while (per > 1 && nbands * ((p.B + per - 1) / per) < 6 * 152) per >>= 1;
+    } else {
+        int dev = 0, sms = 0;
+        cudaError_t ea = cudaGetDevice(&dev);
+        if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (ea != cudaSuccess) return ea;
+        const int64_t slots = 4 * (int64_t)std::max(sms, 1);
+        per = std::max<int64_t>(1, (nbands * p.B + slots - 1) / slots);
+        per = std::min<int64_t>(per, std::min<int64_t>(std::max<int64_t>(p.B, 1), (int64_t)1 << 30));
+    }
     per = std::max<int64_t>(per, (p.B + 65534) / 65535);
     const dim3 grid((unsigned)((ny + rows - 1) / rows), (unsigned)((p.B + per - 1) / per));
     const T *x = (const T *)X;

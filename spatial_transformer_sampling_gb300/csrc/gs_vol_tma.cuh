@@ -58,7 +58,7 @@ vol_tma_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restri
     constexpr int EPC = 16 / E;   // elements per 16 bytes (the box's x origin is a multiple)
     extern __shared__ __align__(128) unsigned char vt_smem[];
     __shared__ AffineMap s_map;
-    __shared__ int s_lo[3], s_ext[3], s_k, s_stages;
+    __shared__ int s_lo[3], s_k, s_stages;
     __shared__ __align__(8) uint64_t full[kVtMaxStages], empty[kVtMaxStages];
 
     const SampleArgs &a = P.a;
@@ -103,20 +103,26 @@ vol_tma_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restri
             map_n = n;
             __syncthreads();
         }
-        if (tid < 3) {
-            // box of input indices along axis d = tid, from the tile's eight corners
-            const int d = tid;
+        if (tid < 32) {
+            // box of input indices: lane 8d + ci takes corner ci of the tile
+            // on axis d (lanes 24..31 repeat axis 2); min and max over the
+            // eight corners by shuffles within each group of eight lanes
+            const int d = min(lane >> 3, 2), ci = lane & 7;
             const int o_hi[3] = {min(oz0 + V.tz, a.out[0]) - 1, min(oy0 + V.ty, Ho) - 1,
                                  min(ox0 + V.tx, Wo) - 1};
             const int o_lo[3] = {oz0, oy0, ox0};
-            int64_t qmin = INT64_MAX, qmax = INT64_MIN;
-            for (int ci = 0; ci < 8; ++ci) {
-                int64_t qq = s_map.cst_q[d];
-                for (int jj = 0; jj < 3; ++jj)
-                    qq += s_map.coef_q[d][jj] * (int64_t)(((ci >> jj) & 1) ? o_hi[jj] : o_lo[jj]);
-                qq >>= 8;
-                qmin = qq < qmin ? qq : qmin;
-                qmax = qq > qmax ? qq : qmax;
+            int64_t qq = s_map.cst_q[d];
+#pragma unroll
+            for (int jj = 0; jj < 3; ++jj)
+                qq += s_map.coef_q[d][jj] * (int64_t)(((ci >> jj) & 1) ? o_hi[jj] : o_lo[jj]);
+            qq >>= 8;
+            int64_t qmin = qq, qmax = qq;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                const int64_t a0 = __shfl_xor_sync(0xffffffffu, qmin, o);
+                const int64_t a1 = __shfl_xor_sync(0xffffffffu, qmax, o);
+                qmin = a0 < qmin ? a0 : qmin;
+                qmax = a1 > qmax ? a1 : qmax;
             }
             const Axis &A = P.ax[d];
             if (a.pad == PAD_REFLECTION && (qmin < A.lo_q || qmax > A.lo_q + A.span_q)) {
@@ -129,25 +135,30 @@ vol_tma_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restri
             int lo = vol_index<MODE>(qmin, A.n);
             const int hi = vol_index<MODE>(qmax, A.n) + (K - 1);
             if (d == 2) lo = (lo >= 0 ? lo : lo - (EPC - 1)) / EPC * EPC;   // 16-byte origin
-            s_lo[d] = lo;
-            s_ext[d] = hi - lo + 1;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            // the smallest box that covers the tile, and the stages that fit
-            int k = -1, stages = 0;
-            if (!s_map.wide) {
-                for (int m = 0; m < V.nmaps && k < 0; ++m)
-                    if (V.box[m][0] >= s_ext[0] && V.box[m][1] >= s_ext[1] && V.box[m][2] >= s_ext[2])
-                        k = m;
-                if (k >= 0) {
-                    const int bytes = (V.box[k][0] * V.box[k][1] * V.box[k][2] * E + 127) & ~127;
-                    stages = min(kVtMaxStages, kVtRingBytes / bytes);
-                    if (stages < 2) stages = 0;
-                }
+            int blo[3], ext[3];
+#pragma unroll
+            for (int dd = 0; dd < 3; ++dd) {
+                blo[dd] = __shfl_sync(0xffffffffu, lo, 8 * dd);
+                ext[dd] = __shfl_sync(0xffffffffu, hi - lo + 1, 8 * dd);
             }
-            s_k = k;
-            s_stages = stages;
+            if (lane == 0) {
+                // the smallest box that covers the tile, and the stages that fit
+                int k = -1, stages = 0;
+                if (!s_map.wide) {
+                    for (int m = 0; m < V.nmaps && k < 0; ++m)
+                        if (V.box[m][0] >= ext[0] && V.box[m][1] >= ext[1] && V.box[m][2] >= ext[2])
+                            k = m;
+                    if (k >= 0) {
+                        const int bytes = (V.box[k][0] * V.box[k][1] * V.box[k][2] * E + 127) & ~127;
+                        stages = min(kVtMaxStages, kVtRingBytes / bytes);
+                        if (stages < 2) stages = 0;
+                    }
+                }
+#pragma unroll
+                for (int dd = 0; dd < 3; ++dd) s_lo[dd] = blo[dd];
+                s_k = k;
+                s_stages = stages;
+            }
         }
         __syncthreads();
         const int S = s_stages;
@@ -199,6 +210,19 @@ vol_tma_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restri
         const uint32_t box_bytes = (uint32_t)bz * dz_b;               // one copy
         const uint32_t stage_bytes = (box_bytes + 127u) & ~127u;      // stage stride
         const int lo_z = s_lo[0], lo_y = s_lo[1], lo_x = s_lo[2];
+        const int C = a.C;
+        const uint32_t ring_u32 = smem_u32(ring);
+        // channel c of this image into stage s (thread 0)
+        auto issue = [&](int c, int s) {
+            mbar_arrive_expect_tx(&full[s], box_bytes);
+            tma_load_4d(ring + (size_t)s * stage_bytes, &maps.m[k], lo_x, lo_y, lo_z, n * C + c,
+                        &full[s]);
+            ipar ^= 1u << s;
+            iany |= 1u << s;
+        };
+        // the first stages are in flight while the taps are set up
+        if (tid == 0)
+            for (int c = 0; c < S && c < C; ++c) issue(c, c);
 
         // this thread's positions: base byte offset in a stage, weights, Y offset
         uint32_t base[kVtPPT];
@@ -247,18 +271,6 @@ vol_tma_kernel(const T *__restrict__ X, const T *__restrict__ theta, T *__restri
             yoff[j] = (opos[0] * Ho + opos[1]) * Wo + opos[2];
         }
 
-        const int C = a.C;
-        const uint32_t ring_u32 = smem_u32(ring);
-        // channel c of this image into stage s (thread 0)
-        auto issue = [&](int c, int s) {
-            mbar_arrive_expect_tx(&full[s], box_bytes);
-            tma_load_4d(ring + (size_t)s * stage_bytes, &maps.m[k], lo_x, lo_y, lo_z, n * C + c,
-                        &full[s]);
-            ipar ^= 1u << s;
-            iany |= 1u << s;
-        };
-        if (tid == 0)
-            for (int c = 0; c < S && c < C; ++c) issue(c, c);
         // a tile inside the output stores every position: no per-position predicate
         const bool full_tile = oz0 + V.tz <= a.out[0] && oy0 + V.ty <= Ho && ox0 + V.tx <= Wo &&
                                V.tz * V.ty * V.tx == kVtTile;

@@ -471,3 +471,33 @@ def test_affine3d_box_too_large_gathers_instead(gs_cuda, oracle_mod, pad):
     assert gs_cuda.gs_device_status() == 0
     assert_parity(Y, oracle_mod.affine_sample(exact(Tt), size, exact(Xt), "linear", pad, 1),
                   "float32", f"3d gather fallback {pad}")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_affine3d_batch_matches_per_image_calls(gs_cuda, oracle_mod, dtype):
+    """More 8 x 8 x 16 output tiles than the persistent grid (two blocks per
+    SM) holds, with a partial last round: blocks take several tiles of
+    different images in turn.  The batched call must give the bits of one call
+    per image (fewer tiles than blocks, one tile each) and agree with the
+    oracle on sampled outputs."""
+    grid = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    tiles_per_image = 4 * 4 * 4                      # output (32, 32, 64)
+    n = next(k for k in range(2, 200)
+             if k * tiles_per_image > grid and 0 < (k * tiles_per_image) % grid <= grid // 3)
+    C = 7
+    g = wl.rng(29)
+    xs = (n, C, 32, 32, 64)
+    size = (n, C, 32, 32, 64)
+    theta = np.tile(np.eye(3, 4), (n, 1, 1)) + g.normal(0.0, 0.05, size=(n, 3, 4))
+    Tt, Xt = wl.as_dtype(theta, dtype), wl.as_dtype(g.normal(size=xs), dtype)
+    Td, Xd = Tt.cuda(), Xt.cuda()
+    Y = gs_cuda.gs_affine_sample(Td, size, Xd, "linear", "zeros", 0)
+    assert gs_cuda.gs_device_status() == 0
+    for i in range(n):
+        Yi = gs_cuda.gs_affine_sample(Td[i:i + 1].contiguous(), (1,) + size[1:],
+                                      Xd[i:i + 1].contiguous(), "linear", "zeros", 0)
+        assert torch.equal(Y[i], Yi[0]), f"image {i} differs from its own call"
+    idx = _sample_idx(Y.numel(), k=5000, seed=4)
+    ref = oracle_mod.affine_sample_at(exact(Tt), size, exact(Xt), idx, "linear", "zeros", 0)
+    assert_parity(Y.reshape(-1)[torch.from_numpy(idx).cuda()], ref, dtype,
+                  f"3d batch {dtype}")
